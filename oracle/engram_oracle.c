@@ -1,0 +1,283 @@
+/*
+ * engram_oracle.c -- plain CPU oracle of the Engram hashed n-gram memory lookup.
+ *
+ * TEST INFRASTRUCTURE ONLY (parity reference; see engram_oracle.h).  Only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg use it.  It shares
+ * nothing with the CUDA library.  Parity pins: tests/test_oracle_pins.py.
+ *
+ * Built with -ffp-contract=off so that no a*b+c is fused: every fp64 operation
+ * below rounds exactly as written, on x86-64 and on AArch64 alike.
+ */
+#include "engram_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* The multiplier of the n-gram fold, fixed by the workload spec. */
+#define ORC_FOLD_MUL 0x9E3779B97F4A7C15ull
+
+/*
+ * splitmix64 (S. Vigna, public domain): the first output of a generator whose
+ * state is x.  The state is advanced by the golden-ratio increment, then mixed
+ * with two xor-shift-multiply rounds and a final xor-shift, all mod 2^64.
+ */
+uint64_t orc_splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+/* Seed of n-gram order n (2, 3 or 4) and hash head j: splitmix64 of n*16 + j. */
+uint64_t orc_seed(int n, int j) { return orc_splitmix64((uint64_t)(n * 16 + j)); }
+
+/*
+ * The hash of one n-gram window (oldest id first), for head j:
+ * h = seed(n, j); for each id e: h = (h xor e) * FOLD_MUL mod 2^64; h ^= h >> 29.
+ * Ids are non-negative and zero-extended to 64 bits.  (VeOmni PR page, commit
+ * "n-gram memory lookup": hash ids per n-gram order and head; the fold itself is
+ * the workload spec's, the pages do not print one.)
+ */
+uint64_t orc_ngram_hash(const int32_t *window, int n, int j) {
+  uint64_t h = orc_seed(n, j);
+  for (int k = 0; k < n; ++k) {
+    h = (h ^ (uint64_t)(uint32_t)window[k]) * ORC_FOLD_MUL;
+    h ^= h >> 29;
+  }
+  return h;
+}
+
+/*
+ * OCP 8-bit floating point, E4M3 "fn" flavour (the pages' fp8_e4m3fn): 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits; no infinities; S.1111.111 is NaN;
+ * exponent field 0 is subnormal: m * 2^-9.  Normal: (1 + m/8) * 2^(e-7).
+ */
+double orc_e4m3fn_decode(uint8_t byte) {
+  int s = byte >> 7;
+  int e = (byte >> 3) & 0xF;
+  int m = byte & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp((double)(8 + m), e - 10); /* (1 + m/8) * 2^(e-7) */
+  return s ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32: widening is exact. */
+double orc_bf16_decode(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/*
+ * Round a double once to the nearest bfloat16, ties to even.  A bfloat16 has 8
+ * significant bits, so inside the binade [2^(e-1), 2^e) its spacing is 2^(e-8);
+ * below the smallest normal 2^-126 the spacing stays at 2^-133.  Scaling by a
+ * power of two is exact, and nearbyint() rounds ties to even in the default
+ * rounding mode.  Results beyond the largest finite bfloat16, (2 - 2^-7) * 2^127,
+ * become infinities.
+ */
+uint16_t orc_bf16_round(double y) {
+  if (isnan(y)) return 0x7FC0;
+  if (isinf(y)) return signbit(y) ? 0xFF80 : 0x7F80;
+  if (y == 0.0) return signbit(y) ? 0x8000 : 0x0000;
+  int e;
+  (void)frexp(fabs(y), &e); /* |y| = f * 2^e, f in [0.5, 1) */
+  int ulp_exp = e - 8;
+  if (ulp_exp < -133) ulp_exp = -133;
+  double r = ldexp(nearbyint(ldexp(y, -ulp_exp)), ulp_exp);
+  if (fabs(r) > 0x1.FEp127) return signbit(y) ? 0xFF80 : 0x7F80;
+  if (r == 0.0) return signbit(y) ? 0x8000 : 0x0000;
+  float f = (float)r; /* exact: r has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+/*
+ * tid2eid compression (VeOmni PR page, PR description and the "n-gram memory
+ * lookup" commit: a persistent many-to-one token_map from tokenizer id to
+ * compressed id).  eid = tid2eid[tid].  A token id outside [0, vocab) or a map
+ * value outside [0, n_eids] leaves that output unwritten and sets a flag.
+ */
+int orc_compress(const int32_t *token_ids, int64_t n, const int32_t *tid2eid, int32_t vocab,
+                 int32_t n_eids, int32_t *eids_out) {
+  int flags = 0;
+  if (n < 0 || vocab < 1 || n_eids < 0) return ORC_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t t = token_ids[i];
+    if (t < 0 || t >= vocab) {
+      flags |= ORC_BAD_TOKEN;
+      continue;
+    }
+    int32_t e = tid2eid[t];
+    if (e < 0 || e > n_eids) {
+      flags |= ORC_BAD_EID;
+      continue;
+    }
+    eids_out[i] = e;
+  }
+  return flags;
+}
+
+/*
+ * The compressed id at position p of sequence b.  Positions before the start of
+ * the call take the caller's history (the last three ids of the earlier
+ * sequence, oldest first) when one is given, else the pad id 0: an n-gram never
+ * reaches past position 0 (VeOmni PR page, "n-gram memory lookup" commit and the
+ * commit on the incremental decode cache: a three-id tail is the whole cache; a
+ * blocked lookback compresses to pad).
+ */
+static int32_t orc_eid_at(const int32_t *eids, int32_t S, const int32_t *history, int32_t b,
+                          int32_t p) {
+  if (p >= 0) return eids[(int64_t)b * S + p];
+  if (history) return history[(int64_t)b * 3 + 3 + p];
+  return 0;
+}
+
+/*
+ * Hash ids [B, S, 3, H] (n-major: index ((b*S + s)*3 + (n-2))*H + j) for the
+ * 2-, 3- and 4-gram ending at every position (NeMo AutoModel page,
+ * DeepseekV41Block.forward: engram_hash_ids [batch, sequence, hash_heads]).  The
+ * window of order n at position s is the ids at s-n+1 .. s, oldest first.
+ * row = h mod rows_n, unsigned, on the full 64-bit h.  A negative id anywhere in
+ * the 4-id window s-3 .. s leaves all 3H ids of that token unwritten and sets a
+ * flag.  history_out (optional) receives the last three ids of history ++ eids,
+ * oldest first: the next call's history.
+ */
+int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
+             int32_t n_heads, const int64_t rows[3], int32_t *row_ids_out,
+             int32_t *history_out) {
+  if (B < 0 || S < 0 || n_heads < 1) return ORC_BAD_ARG;
+  for (int n = 0; n < 3; ++n)
+    if (rows[n] < 1) return ORC_BAD_ARG;
+  const int64_t T = (int64_t)B * S;
+  const int R = 3 * n_heads;
+  int flags = 0;
+#pragma omp parallel for schedule(static) reduction(| : flags)
+  for (int64_t t = 0; t < T; ++t) {
+    int32_t b = (int32_t)(t / S), s = (int32_t)(t % S);
+    int32_t w4[4];
+    int bad = 0;
+    for (int k = 0; k < 4; ++k) {
+      w4[k] = orc_eid_at(eids, S, history, b, s - 3 + k);
+      if (w4[k] < 0) bad = 1;
+    }
+    if (bad) {
+      flags |= ORC_BAD_EID;
+      continue;
+    }
+    for (int n = 2; n <= 4; ++n) {
+      const int32_t *window = w4 + (4 - n); /* ids at s-n+1 .. s */
+      for (int j = 0; j < n_heads; ++j) {
+        uint64_t h = orc_ngram_hash(window, n, j);
+        row_ids_out[t * R + (int64_t)(n - 2) * n_heads + j] = (int32_t)(h % (uint64_t)rows[n - 2]);
+      }
+    }
+  }
+  if (history_out) {
+    for (int32_t b = 0; b < B; ++b) {
+      int32_t tail[3];
+      for (int k = 0; k < 3; ++k) tail[k] = orc_eid_at(eids, S, history, b, S - 3 + k);
+      for (int k = 0; k < 3; ++k) history_out[(int64_t)b * 3 + k] = tail[k];
+    }
+  }
+  return flags;
+}
+
+/*
+ * The fused lookup for n_tokens tokens, one at a time, in fp64:
+ *  1. gather + dequantise the 3H rows of the token: FP8 byte decoded exactly,
+ *     times the row's fp32 scale (VeOmni PR page: FP8 tables with row-wise
+ *     dequantisation on lookup), or the BF16 value widened exactly;
+ *  2. m = (sum of the 3H rows) / (3H)  (workload spec: the mean of the rows);
+ *  3. with a = stream 0 of the token:
+ *     g = sigmoid( sum(a*m) / (sqrt(mean(a^2)+eps) * sqrt(mean(m^2)+eps) * sqrt(D)) ),
+ *     which is <rmsnorm(a), rmsnorm(m)> / sqrt(D) with unit RMSNorm weights;
+ *  4. out_s = bf16_round(stream_s + g * alpha_s * m), rounded once, for the four
+ *     streams [tokens, 4, D] (VeOmni PR page: the Engram write goes into the mHC
+ *     streams before its layer; NeMo AutoModel page: streams [batch, sequence,
+ *     streams, hidden]).
+ * A row id outside [0, rows_n) leaves the token's outputs unwritten and sets a
+ * flag.  gate_out [n_tokens] and mem_out [n_tokens, D] are optional.
+ */
+int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
+               int32_t D, const void *const tables[3], const float *const scales[3],
+               const int64_t rows[3], const uint16_t *streams_in, const float *alpha,
+               double eps, uint16_t *streams_out, double *gate_out, double *mem_out) {
+  if (n_tokens < 0 || n_heads < 1 || D < 1) return ORC_BAD_ARG;
+  if (dtype != ORC_FP8_E4M3FN && dtype != ORC_BF16) return ORC_BAD_ARG;
+  const int R = 3 * n_heads;
+  int flags = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : flags)
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int32_t *ids = row_ids + t * R;
+    int bad = 0;
+    for (int r = 0; r < R; ++r) {
+      int n = r / n_heads;
+      if (ids[r] < 0 || (int64_t)ids[r] >= rows[n]) bad = 1;
+    }
+    if (bad) {
+      flags |= ORC_BAD_ROW;
+      continue;
+    }
+    double *m = (double *)calloc((size_t)D, sizeof(double));
+    for (int r = 0; r < R; ++r) {
+      int n = r / n_heads;
+      int64_t row = ids[r];
+      for (int i = 0; i < D; ++i) {
+        double v;
+        if (dtype == ORC_FP8_E4M3FN) {
+          const uint8_t *tab = (const uint8_t *)tables[n];
+          v = orc_e4m3fn_decode(tab[row * D + i]) * (double)scales[n][row];
+        } else {
+          const uint16_t *tab = (const uint16_t *)tables[n];
+          v = orc_bf16_decode(tab[row * D + i]);
+        }
+        m[i] += v;
+      }
+    }
+    for (int i = 0; i < D; ++i) m[i] /= (double)R;
+
+    const uint16_t *x = streams_in + t * 4 * (int64_t)D;
+    double saa = 0.0, smm = 0.0, sam = 0.0;
+    for (int i = 0; i < D; ++i) {
+      double a = orc_bf16_decode(x[i]);
+      saa += a * a;
+      smm += m[i] * m[i];
+      sam += a * m[i];
+    }
+    double rms_a = sqrt(saa / D + eps);
+    double rms_m = sqrt(smm / D + eps);
+    double logit = sam / (rms_a * rms_m * sqrt((double)D));
+    double g = 1.0 / (1.0 + exp(-logit));
+
+    uint16_t *y = streams_out + t * 4 * (int64_t)D;
+    for (int s = 0; s < 4; ++s)
+      for (int i = 0; i < D; ++i) {
+        double xi = orc_bf16_decode(x[(int64_t)s * D + i]);
+        y[(int64_t)s * D + i] = orc_bf16_round(xi + g * (double)alpha[s] * m[i]);
+      }
+    if (gate_out) gate_out[t] = g;
+    if (mem_out)
+      for (int i = 0; i < D; ++i) mem_out[t * D + i] = m[i];
+    free(m);
+  }
+  return flags;
+}
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
