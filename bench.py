@@ -1,0 +1,493 @@
+"""Benchmark of the Engram hashed n-gram memory lookup on GB300.
+
+One step = the whole hot path over one batch: engram_compress -> engram_hash ->
+engram_lookup_fused, through the C ABI, on the full-size prefill workload
+(batch 8 x seq 8192 tokens, 8 hash heads, 4096-wide rows, three 5,040,000-row
+FP8 e4m3fn tables with fp32 row scales = 57.7 GiB, bf16 streams [8, 8192, 4, 4096]).
+Inputs are resident in HBM when the timed region starts; every input is larger
+than the 129 MB L2 (no flush needed).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+For N > 1 (torchrun, one rank per GPU) every rank holds a replica of the tables
+and processes its own batch (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "full_prefill_fp8"
+METRIC = "Engram fused lookup tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lookup_fused_traffic.json")
+LOOKUP_SRC = os.path.join(ROOT, "hashed_gram_memory_gb300", "csrc", "lookup_fused.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[c.name for c in W.CONFIGS])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def config_of(name: str) -> W.EngramConfig:
+    return next(c for c in W.CONFIGS if c.name == name)
+
+
+def workload_desc(cfg: W.EngramConfig) -> dict:
+    return {
+        "workload": cfg.name,
+        "batch": cfg.B, "seq": cfg.S, "tokens_per_step": cfg.T, "hash_heads": cfg.H, "D": cfg.D,
+        "table_rows": list(cfg.rows), "table_dtype": cfg.dtype,
+        "table_bytes": cfg.table_bytes(), "token_ids": cfg.ids,
+        "repeated_4gram_frac": cfg.repeat_frac, "decode_history": cfg.decode,
+        "l2": "no flush: every input is larger than the 129 MB L2 "
+              f"(tables {cfg.table_bytes() / 2**30:.1f} GiB, streams "
+              f"{cfg.T * 4 * cfg.D * 2 / 1e9:.2f} GB in + out per step)",
+        "parallelism": "replicas (weak scaling, no data-path collective)",
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(cfg):
+    """Per-launch DRAM bytes of the lookup kernel from the committed ncu summary,
+    or None when the kernel source changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    sha = hashlib.sha256(open(LOOKUP_SRC, "rb").read()).hexdigest()
+    rec = d.get(cfg.name)
+    if not rec or rec.get("lookup_fused_cu_sha256") != sha:
+        return None
+    return float(rec["dram_bytes_per_token"]) * cfg.T
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the GPU's clocks and throttle reasons."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        sel = []
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            uuid = str(getattr(props, "uuid", ""))
+            if uuid:
+                sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        cmd = ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+               "-lms", "100"] + sel
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s.split(", ") for (t, s) in self.samples if t0 <= t <= t1]
+        rows = [r for r in rows if len(r) == len(self.FIELDS)]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].strip() == "Active"})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------- native arm
+
+def device_inputs(eg, cfg, rank, device):
+    import torch
+    tabs, scales = W.tables_device(cfg, device)
+    dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
+    hist = W.history(cfg, rank)
+    return dict(
+        ids=torch.from_numpy(W.token_ids(cfg, rank)).to(device),
+        tid2eid=torch.from_numpy(W.tid2eid(cfg)).to(device),
+        history=None if hist is None else torch.from_numpy(hist).to(device),
+        streams=W.streams_device(cfg, device, rank),
+        alpha=torch.from_numpy(W.alpha(cfg)).to(device),
+        tables=eg.Tables(dt, tabs, scales),
+    )
+
+
+class Step:
+    """Pre-allocated buffers and the three C-ABI calls of one step."""
+
+    def __init__(self, eg, cfg, d, stream):
+        import torch
+        self.eg, self.cfg, self.d, self.stream = eg, cfg, d, stream
+        dev = d["streams"].device
+        self.eids = torch.empty_like(d["ids"])
+        self.rows = torch.empty((cfg.B, cfg.S, 3, cfg.H), dtype=torch.int32, device=dev)
+        self.hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
+        self.out = torch.empty_like(d["streams"])
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.launches = 3
+
+    def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None):
+        eg, cfg, d = self.eg, self.cfg, self.d
+        ids = d["ids"] if ids is None else ids
+        x = d["streams"] if x is None else x
+        out = self.out if out is None else out
+        eg.engram_compress(ids, d["tid2eid"], cfg.n_eids, eids_out=self.eids, status=self.status,
+                           stream=self.stream)
+        eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
+                       row_ids_out=self.rows, status=self.status, stream=self.stream)
+        if ev_start is not None:
+            ev_start.record(self.stream)
+        eg.engram_lookup_fused(self.rows, cfg.H, d["tables"], x, d["alpha"], cfg.eps,
+                               streams_out=out, status=self.status, stream=self.stream)
+        if ev_end is not None:
+            ev_end.record(self.stream)
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+    import hashed_gram_memory_gb300 as eg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    cfg = config_of(args.workload)
+    d = device_inputs(eg, cfg, rank, device)
+    stream = torch.cuda.Stream(device)
+    step = Step(eg, cfg, d, stream)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize()
+    code, flags = eg.engram_read_status(step.status, stream)
+    if flags:
+        raise SystemExit(f"device status flags 0x{flags:x} during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_begin.record(stream)
+    for i in range(K):
+        step(ev[i][0], ev[i][1])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = t_begin.elapsed_time(t_end)
+    lookup_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    code, flags = eg.engram_read_status(step.status, stream)
+    clk = clocks.summary(wall0, wall1) if clocks else None
+    if clocks:
+        clocks.stop()
+
+    e2e = None if args.no_e2e else run_e2e(eg, cfg, step, stream, args.e2e_steps, world, device)
+    cpu = None if (args.no_cpu_baseline or rank != 0) else cpu_baseline(cfg, d, args.cpu_sample_tokens)
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        bytes_tok = cfg.algorithmic_bytes_per_token()
+        lk = statistics.mean(lookup_ms)
+        achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
+        traffic = recorded_traffic(cfg)
+        value = world * cfg.T * K / (ms_total * 1e-3)
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": ms_total / K,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded; tables and streams generated on the GPU)",
+            "config": workload_desc(cfg),
+            "hbm_gbs_effective_step": bytes_tok * cfg.T * K / (ms_total * 1e-3) / 1e9,
+            "roofline": {
+                "kernel": "engram_lookup_fused",
+                "bound": "hbm",
+                "achieved": achieved,
+                "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": traffic,
+                "algorithmic_bytes_per_token": bytes_tok,
+                "lookup_ms_mean": lk,
+                "lookup_ms_median": statistics.median(lookup_ms),
+            },
+            "gpu_launches": step.launches * K,
+            "status_flags": flags,
+            "clocks": clk,
+        }
+        if e2e:
+            line["e2e"] = e2e
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(eg, cfg, step, stream, steps, world, device):
+    """Same metric through the C ABI with host buffers: every step copies the token
+    ids and the four input streams from pinned host memory, runs the three calls,
+    and copies the updated streams back, all inside the timed region."""
+    import torch
+    import torch.distributed as dist
+    d = step.d
+    ids_h = d["ids"].cpu().pin_memory()
+    x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    x_h.copy_(d["streams"])
+    y_h = torch.empty_like(x_h, pin_memory=True)
+    ids_d = torch.empty_like(d["ids"])
+    x_d = torch.empty_like(d["streams"])
+    y_d = torch.empty_like(d["streams"])
+
+    def one():
+        ids_d.copy_(ids_h, non_blocking=True)
+        x_d.copy_(x_h, non_blocking=True)
+        step(ids=ids_d, x=x_d, out=y_d)
+        y_h.copy_(y_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            one()
+    stream.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([dt], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        dt = float(tt.item())
+    h2d = ids_h.numel() * 4 + x_h.numel() * 2
+    d2h = y_h.numel() * 2
+    return {"value": world * cfg.T * steps / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "how": "pinned host ids + streams -> device, compress/hash/lookup, streams -> host; "
+                   "one CUDA stream, timed on the host around the steps"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_sample(cfg, d, n_tokens):
+    """Host inputs for the first n_tokens tokens of sequence 0 (self-contained
+    windows), with exactly the table rows they need copied back from the device."""
+    import torch
+    import oracle
+    n = min(n_tokens, cfg.S) if not cfg.decode else min(n_tokens, cfg.B)
+    if cfg.decode:
+        ids = d["ids"][:n].cpu().numpy()
+        hist = d["history"][:n].cpu().numpy()
+        x = d["streams"][:n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
+    else:
+        ids = d["ids"][:1, :n].cpu().numpy()
+        hist = None
+        x = d["streams"][0, :n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
+    tid2eid = d["tid2eid"].cpu().numpy()
+    e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
+    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist)
+    r = r.reshape(n, -1)
+    # full-size host copies are too large: the oracle gets tables holding only the
+    # rows the sample needs, with the row ids remapped onto them
+    host_tabs, host_scales, remap = [], [], np.empty_like(r)
+    for k in range(3):
+        cols = slice(k * cfg.H, (k + 1) * cfg.H)
+        uniq, inv = np.unique(r[:, cols], return_inverse=True)
+        remap[:, cols] = inv.reshape(r[:, cols].shape)
+        idx = torch.from_numpy(uniq.astype(np.int64)).to(d["tables"].tables[k].device)
+        t = d["tables"].tables[k].index_select(0, idx).cpu().numpy()
+        host_tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))
+        host_scales.append(d["tables"].scales[k].index_select(0, idx).cpu().numpy()
+                           if cfg.dtype == W.FP8 else None)
+    return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=x, tables=host_tabs, scales=host_scales,
+                remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n)
+
+
+def time_oracle(cfg, s, repeats=1):
+    """Oracle compress + hash + lookup on the sample; returns seconds per pass."""
+    import oracle
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        e, _ = oracle.compress(s["ids"], s["tid2eid"], cfg.n_eids)
+        oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"])
+        oracle.lookup(s["remap"], cfg.H, oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16,
+                      s["tables"], s["scales"], s["x"], s["alpha"], cfg.eps)
+    return (time.perf_counter() - t0) / repeats
+
+
+def cpu_baseline(cfg, d, n_tokens):
+    import oracle
+    s = oracle_sample(cfg, d, n_tokens)
+    dt = time_oracle(cfg, s)
+    return {"value": s["n"] / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {s['n']} tokens of the {cfg.name} batch (same seeded inputs, the "
+                      f"rows they need copied from the device): compress + hash + fused lookup in "
+                      f"the fp64 C oracle, {dt:.2f} s wall"}
+
+
+def reference_sample(cfg, n):
+    """Host inputs for n tokens of the workload (same distributions, seeded): ids,
+    map, streams, and tables holding just the rows those tokens hash to."""
+    import oracle
+    sub = cfg.scaled(B=1, S=n) if not cfg.decode else cfg.scaled(B=n)
+    ids = W.token_ids(sub)
+    tid2eid = W.tid2eid(cfg)
+    hist = W.history(sub)
+    e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
+    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist)
+    r = r.reshape(n, -1)
+    g = np.random.default_rng([cfg.seed, 99])
+    tabs, scs, remap = [], [], np.empty_like(r)
+    for k in range(3):
+        cols = slice(k * cfg.H, (k + 1) * cfg.H)
+        uniq, inv = np.unique(r[:, cols], return_inverse=True)
+        remap[:, cols] = inv.reshape(r[:, cols].shape)
+        x = g.standard_normal((len(uniq), cfg.D), dtype=np.float32)
+        if cfg.dtype == W.FP8:
+            tabs.append(W._to_e4m3_bytes(x))
+            scs.append(g.uniform(cfg.scale_lo, cfg.scale_hi, len(uniq)).astype(np.float32))
+        else:
+            tabs.append(W._to_bf16_bits(x * np.float32(cfg.bf16_std)))
+            scs.append(None)
+    return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=W.streams_host(sub).reshape(n, 4, cfg.D),
+                tables=tabs, scales=scs, remap=remap, alpha=W.alpha(cfg), n=n)
+
+
+def run_reference(args, budget_s: float = 60.0):
+    """The oracle as it stands on the host cores (rank 0 only), same metric.  Each
+    of the K timed steps runs a bounded sample of the workload, sized from a
+    warm-up pass so that the K steps take about budget_s seconds."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    cfg = config_of(args.workload)
+    K = max(1, args.steps)
+    probe = reference_sample(cfg, min(256, cfg.T))
+    rate = probe["n"] / time_oracle(cfg, probe)
+    n = int(max(16, min(cfg.T, 4096, budget_s * rate / K)))
+    s = reference_sample(cfg, n)
+    for _ in range(max(1, min(args.warmup, 3))):
+        time_oracle(cfg, s)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        time_oracle(cfg, s)
+    dt = (time.perf_counter() - t0) / K
+    value = n / dt
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": K,
+        "warmup": max(1, min(args.warmup, 3)), "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": workload_desc(cfg),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: {n} of the {cfg.T} tokens of {cfg.name} through the "
+                                   "fp64 C oracle (compress + hash + fused lookup), with tables "
+                                   "holding the rows those tokens need"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+"""Engram hashed n-gram memory lookup for GB300 (sm_103a).
+
+A thin Python binding over libengram.so, whose C ABI is include/engram.h.  The
+functions carry the C names and only marshal arguments: torch tensors become
+device pointers, the current torch CUDA stream becomes the cudaStream_t, and a
+non-zero status becomes an EngramError.  Every step of the path runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and importing this
+package fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libengram.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_TIMEOUT = range(6)
+FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
+TABLE_FP8_E4M3FN, TABLE_BF16 = 0, 1
+MAX_HEADS, MAX_D = 32, 4096
+
+
+class EngramError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(message)
+        self.code = code
+
+
+class engram_tables(C.Structure):
+    _fields_ = [("dtype", C.c_int32), ("D", C.c_int32), ("rows", C.c_int64 * 3),
+                ("table", C.c_void_p * 3), ("scale", C.c_void_p * 3)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -m hashed_gram_memory_gb300.build, or __graft_entry__.build())")
+    L = C.CDLL(LIB_PATH)
+    vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+    L.engram_compress.argtypes = [vp, i64, vp, i32, i32, vp, vp, vp]
+    L.engram_hash.argtypes = [vp, i32, i32, vp, vp, i32, C.POINTER(C.c_int64), vp, vp, vp]
+    L.engram_lookup_fused.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, vp, vp,
+                                      C.c_float, vp, vp, vp, vp]
+    L.engram_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
+    for f in ("engram_compress", "engram_hash", "engram_lookup_fused", "engram_read_status"):
+        getattr(L, f).restype = C.c_int32
+    L.engram_status_string.argtypes = [C.c_int32]
+    L.engram_status_string.restype = C.c_char_p
+    L.engram_last_error.argtypes = []
+    L.engram_last_error.restype = C.c_char_p
+    L.engram_abi_version.restype = C.c_int32
+    return L
+
+
+lib = _load()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        msg = lib.engram_last_error().decode() or lib.engram_status_string(code).decode()
+        raise EngramError(code, f"{what}: {lib.engram_status_string(code).decode()}: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtypes, name, contiguous=True):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise EngramError(ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise EngramError(ERR_INVALID_ARG, f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if contiguous and not t.is_contiguous():
+        raise EngramError(ERR_INVALID_ARG, f"{name} must be contiguous")
+
+
+@dataclasses.dataclass
+class Tables:
+    """The three device tables (orders 2, 3, 4) and, for FP8, their fp32 row scales."""
+
+    dtype: int
+    tables: list
+    scales: list | None = None
+
+    @property
+    def D(self) -> int:
+        return int(self.tables[0].shape[1])
+
+    @property
+    def rows(self):
+        return [int(t.shape[0]) for t in self.tables]
+
+    def struct(self) -> engram_tables:
+        s = engram_tables()
+        s.dtype = self.dtype
+        s.D = self.D
+        for n in range(3):
+            s.rows[n] = int(self.tables[n].shape[0])
+            s.table[n] = self.tables[n].data_ptr()
+            s.scale[n] = self.scales[n].data_ptr() if self.scales else None
+        return s
+
+
+def engram_compress(token_ids, tid2eid, n_eids: int, eids_out=None, status=None, stream=None):
+    """eids_out[i] = tid2eid[token_ids[i]] (int32, same shape as token_ids)."""
+    import torch
+    _need(token_ids, (torch.int32,), "token_ids")
+    _need(tid2eid, (torch.int32,), "tid2eid")
+    if eids_out is None:
+        eids_out = torch.empty_like(token_ids)
+    _need(eids_out, (torch.int32,), "eids_out")
+    _check(lib.engram_compress(_ptr(token_ids), token_ids.numel(), _ptr(tid2eid), tid2eid.numel(),
+                               n_eids, _ptr(eids_out), _ptr(status), _stream(stream)),
+           "engram_compress")
+    return eids_out
+
+
+def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_ids_out=None,
+                status=None, stream=None):
+    """Row ids [B, S, 3, n_heads] int32 for eids [B, S]; history/history_out [B, 3]."""
+    import torch
+    _need(eids, (torch.int32,), "eids")
+    if eids.dim() != 2:
+        raise EngramError(ERR_INVALID_ARG, "eids must be [batch, seq]")
+    B, S = eids.shape
+    if row_ids_out is None:
+        row_ids_out = torch.empty((B, S, 3, n_heads), dtype=torch.int32, device=eids.device)
+    _need(row_ids_out, (torch.int32,), "row_ids_out")
+    _need(history, (torch.int32,), "history")
+    _need(history_out, (torch.int32,), "history_out")
+    r = (C.c_int64 * 3)(*[int(x) for x in rows])
+    _check(lib.engram_hash(_ptr(eids), B, S, _ptr(history), _ptr(history_out), n_heads, r,
+                           _ptr(row_ids_out), _ptr(status), _stream(stream)), "engram_hash")
+    return row_ids_out
+
+
+def engram_lookup_fused(row_ids, n_heads: int, tables: Tables, streams_in, alpha,
+                        eps: float = 1e-6, streams_out=None, gate_out=None, mem_out=None,
+                        status=None, stream=None):
+    """The fused gather / mean / gate / add.  streams_in: bf16 [..., 4, D]; returns streams_out."""
+    import torch
+    _need(row_ids, (torch.int32,), "row_ids")
+    bf = (torch.bfloat16, torch.int16)
+    _need(streams_in, bf, "streams_in")
+    _need(alpha, (torch.float32,), "alpha")
+    D = tables.D
+    if streams_in.shape[-2:] != (4, D):
+        raise EngramError(ERR_INVALID_ARG, f"streams_in must be [..., 4, {D}]")
+    T = streams_in.numel() // (4 * D)
+    if row_ids.numel() != T * 3 * n_heads:
+        raise EngramError(ERR_INVALID_ARG, "row_ids and streams disagree on the token count")
+    if streams_out is None:
+        streams_out = torch.empty_like(streams_in)
+    _need(streams_out, bf, "streams_out")
+    _need(gate_out, (torch.float32,), "gate_out")
+    _need(mem_out, (torch.float32,), "mem_out")
+    s = tables.struct()
+    _check(lib.engram_lookup_fused(_ptr(row_ids), T, n_heads, C.byref(s), _ptr(streams_in),
+                                   _ptr(streams_out), _ptr(alpha), float(eps), _ptr(gate_out),
+                                   _ptr(mem_out), _ptr(status), _stream(stream)),
+           "engram_lookup_fused")
+    return streams_out
+
+
+def engram_read_status(status, stream=None):
+    """(code, flags): waits for the stream and reads the device status word."""
+    v = C.c_int32(0)
+    code = lib.engram_read_status(_ptr(status), C.byref(v), _stream(stream))
+    if code not in (OK, ERR_OUT_OF_RANGE, ERR_TIMEOUT):
+        _check(code, "engram_read_status")
+    return code, int(v.value)
+
+
+def engram_status_string(code: int) -> str:
+    return lib.engram_status_string(code).decode()
+
+
+def engram_abi_version() -> int:
+    return int(lib.engram_abi_version())

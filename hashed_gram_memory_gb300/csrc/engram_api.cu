@@ -1,0 +1,253 @@
+// engram_api.cu -- the extern "C" entry points of libengram (include/engram.h):
+// argument validation on the host, the device check, the launches, and the
+// status-word read-back.  Every argument error is reported before any launch.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "engram_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+engram_status fail(engram_status code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+engram_status ok() {
+  g_last_error[0] = '\0';
+  return ENGRAM_OK;
+}
+
+engram_status cuda_fail(const char *what, cudaError_t e) {
+  return fail(ENGRAM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return na && nb && x < y + nb && y < x + na;
+}
+
+// Per-device memo of the architecture check: 0 unknown, 1 sm_103, 2 other.
+std::atomic<int> g_arch_ok[64];
+
+engram_status check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("cudaGetDevice", e);
+  const int slot = dev & 63;
+  int known = g_arch_ok[slot].load(std::memory_order_relaxed);
+  if (known == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail("cudaDeviceGetAttribute", e);
+    known = (major == 10 && minor == 3) ? 1 : 2;
+    g_arch_ok[slot].store(known, std::memory_order_relaxed);
+    if (known == 2)
+      return fail(ENGRAM_ERR_UNSUPPORTED, "device %d is sm_%d%d; libengram is built for sm_103a",
+                  dev, major, minor);
+  }
+  if (known == 2) return fail(ENGRAM_ERR_UNSUPPORTED, "device %d is not sm_103", dev);
+  return ENGRAM_OK;
+}
+
+engram_status launched(const char *what, cudaError_t e) {
+  if (e != cudaSuccess) return cuda_fail(what, e);
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+ENGRAM_API int32_t engram_abi_version(void) { return ENGRAM_ABI_VERSION; }
+
+ENGRAM_API const char *engram_last_error(void) { return g_last_error; }
+
+ENGRAM_API const char *engram_status_string(engram_status code) {
+  switch (code) {
+    case ENGRAM_OK: return "ENGRAM_OK";
+    case ENGRAM_ERR_INVALID_ARG: return "ENGRAM_ERR_INVALID_ARG: invalid argument";
+    case ENGRAM_ERR_UNSUPPORTED: return "ENGRAM_ERR_UNSUPPORTED: unsupported device or size";
+    case ENGRAM_ERR_CUDA: return "ENGRAM_ERR_CUDA: CUDA runtime error";
+    case ENGRAM_ERR_OUT_OF_RANGE: return "ENGRAM_ERR_OUT_OF_RANGE: an input id was out of range";
+    case ENGRAM_ERR_TIMEOUT: return "ENGRAM_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "ENGRAM: unknown status code";
+  }
+}
+
+ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tokens,
+                                         const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
+                                         int32_t *eids_out, int32_t *status, void *stream) {
+  if (n_tokens < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_tokens < 0");
+  if (vocab < 1) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: vocab < 1");
+  if (n_eids < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_eids < 0");
+  if (!tid2eid) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: tid2eid is NULL");
+  if (n_tokens > 0 && (!token_ids || !eids_out))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: token_ids or eids_out is NULL");
+  if (!aligned(token_ids, 4) || !aligned(tid2eid, 4) || !aligned(eids_out, 4) || !aligned(status, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: int32 pointers must be 4-byte aligned");
+  if (token_ids != eids_out && overlap(token_ids, n_tokens * 4, eids_out, n_tokens * 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: token_ids and eids_out overlap partially");
+  if (overlap(tid2eid, (size_t)vocab * 4, eids_out, n_tokens * 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: eids_out overlaps tid2eid");
+  if (n_tokens == 0) return ok();
+  engram_status st = check_device();
+  if (st != ENGRAM_OK) return st;
+  engram::CompressParams p{token_ids, n_tokens, tid2eid, vocab, n_eids, eids_out, status};
+  return launched("engram_compress launch", engram::launch_compress(p, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,
+                                     const int32_t *history, int32_t *history_out,
+                                     int32_t n_heads, const int64_t *rows_host,
+                                     int32_t *row_ids_out, int32_t *status, void *stream) {
+  if (batch < 0 || seq < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: batch or seq < 0");
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: n_heads must be in [1, %d]", ENGRAM_MAX_HEADS);
+  if (!rows_host) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows_host is NULL");
+  for (int n = 0; n < 3; ++n)
+    if (rows_host[n] < 1 || rows_host[n] > INT32_MAX)
+      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows[%d] must be in [1, 2^31-1]", n);
+  const int64_t T = (int64_t)batch * seq;
+  const size_t R = 3 * (size_t)n_heads;
+  if (T > 0 && (!eids || !row_ids_out))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: eids or row_ids_out is NULL");
+  if (!aligned(eids, 4) || !aligned(history, 4) || !aligned(history_out, 4) ||
+      !aligned(row_ids_out, 4) || !aligned(status, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: int32 pointers must be 4-byte aligned");
+  if (overlap(eids, T * 4, row_ids_out, T * R * 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: row_ids_out overlaps eids");
+  if (history_out) {
+    const size_t hb = (size_t)batch * 3 * 4;
+    if (overlap(history_out, hb, eids, T * 4) || overlap(history_out, hb, row_ids_out, T * R * 4))
+      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: history_out overlaps eids or row_ids_out");
+    if (history && history != history_out && overlap(history, hb, history_out, hb))
+      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: history and history_out overlap partially");
+  }
+  if (history && overlap(history, (size_t)batch * 12, row_ids_out, T * R * 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: row_ids_out overlaps history");
+  if (T == 0 && (!history_out || batch == 0)) return ok();
+  engram_status st = check_device();
+  if (st != ENGRAM_OK) return st;
+  engram::HashParams p;
+  memset(&p, 0, sizeof p);
+  p.eids = eids;
+  p.history = history;
+  p.history_out = history_out;
+  p.row_ids = row_ids_out;
+  p.status = status;
+  p.T = T;
+  p.batch = batch;
+  p.seq = seq;
+  p.H = n_heads;
+  for (int n = 0; n < 3; ++n) {
+    p.rows[n] = (uint64_t)rows_host[n];
+    for (int j = 0; j < n_heads; ++j) p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
+  }
+  return launched("engram_hash launch", engram::launch_hash(p, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
+                                             int32_t n_heads, const engram_tables *tables_host,
+                                             const uint16_t *streams_in, uint16_t *streams_out,
+                                             const float *alpha, float eps, float *gate_out,
+                                             float *mem_out, int32_t *status, void *stream) {
+  const char *fn = "engram_lookup_fused";
+  if (n_tokens < 0) return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens < 0", fn);
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
+  if (!tables_host) return fail(ENGRAM_ERR_INVALID_ARG, "%s: tables is NULL", fn);
+  const engram_tables &tb = *tables_host;
+  if (tb.dtype != ENGRAM_TABLE_FP8_E4M3FN && tb.dtype != ENGRAM_TABLE_BF16)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: unknown table dtype %d", fn, tb.dtype);
+  if (tb.D < 16 || tb.D % 16 != 0)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: D = %d must be a positive multiple of 16", fn, tb.D);
+  if (tb.D > ENGRAM_MAX_D)
+    return fail(ENGRAM_ERR_UNSUPPORTED, "%s: D = %d exceeds %d", fn, tb.D, ENGRAM_MAX_D);
+  const int D = tb.D;
+  const size_t elt = tb.dtype == ENGRAM_TABLE_FP8_E4M3FN ? 1 : 2;
+  for (int n = 0; n < 3; ++n) {
+    if (tb.rows[n] < 1 || tb.rows[n] > INT32_MAX)
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: rows[%d] must be in [1, 2^31-1]", fn, n);
+    if (!tb.table[n] || !aligned(tb.table[n], 16))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: table[%d] NULL or not 16-byte aligned", fn, n);
+    if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN && (!tb.scale[n] || !aligned(tb.scale[n], 4)))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: scale[%d] NULL or not 4-byte aligned", fn, n);
+  }
+  if (!alpha || !aligned(alpha, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: alpha NULL or not 4-byte aligned", fn);
+  if (!(eps >= 0.f) || !isfinite(eps))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", fn);
+  const size_t R = 3 * (size_t)n_heads;
+  const size_t sbytes = (size_t)n_tokens * 4 * D * 2;
+  if (n_tokens > 0) {
+    if (!row_ids || !streams_in || !streams_out)
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids or streams is NULL", fn);
+    if (!aligned(row_ids, 4) || !aligned(status, 4) || !aligned(gate_out, 4))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids/status/gate_out not 4-byte aligned", fn);
+    if (!aligned(streams_in, 16) || !aligned(streams_out, 16) || !aligned(mem_out, 16))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: streams and mem_out must be 16-byte aligned", fn);
+    if (streams_in != streams_out && overlap(streams_in, sbytes, streams_out, sbytes))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: streams_out overlaps streams_in partially", fn);
+    const size_t ib = n_tokens * R * 4;
+    if (overlap(streams_out, sbytes, row_ids, ib) ||
+        (mem_out && overlap(mem_out, (size_t)n_tokens * D * 4, streams_out, sbytes)) ||
+        (gate_out && overlap(gate_out, (size_t)n_tokens * 4, streams_out, sbytes)))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: output buffers overlap", fn);
+    for (int n = 0; n < 3; ++n)
+      if (overlap(streams_out, sbytes, tb.table[n], (size_t)tb.rows[n] * D * elt))
+        return fail(ENGRAM_ERR_INVALID_ARG, "%s: streams_out overlaps table[%d]", fn, n);
+  }
+  if (n_tokens == 0) return ok();
+  engram_status st = check_device();
+  if (st != ENGRAM_OK) return st;
+  engram::LookupParams p;
+  memset(&p, 0, sizeof p);
+  p.row_ids = row_ids;
+  for (int n = 0; n < 3; ++n) {
+    p.table[n] = static_cast<const uint8_t *>(tb.table[n]);
+    p.scale[n] = tb.scale[n];
+    p.rows[n] = tb.rows[n];
+  }
+  p.x = streams_in;
+  p.y = streams_out;
+  p.alpha = alpha;
+  p.gate_out = gate_out;
+  p.mem_out = mem_out;
+  p.status = status;
+  p.T = n_tokens;
+  p.H = n_heads;
+  p.D = D;
+  p.eps = eps;
+  return launched("engram_lookup_fused launch",
+                  engram::launch_lookup(p, tb.dtype, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flags_host,
+                                            void *stream) {
+  if (!status || !flags_host)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_read_status: NULL pointer");
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail("engram_read_status", e);
+  *flags_host = v;
+  if (v & ENGRAM_FLAG_TIMEOUT) return fail(ENGRAM_ERR_TIMEOUT, "status word 0x%x", v);
+  if (v) return fail(ENGRAM_ERR_OUT_OF_RANGE, "status word 0x%x", v);
+  return ok();
+}
+
+}  // extern "C"

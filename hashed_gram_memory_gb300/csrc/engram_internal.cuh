@@ -1,0 +1,66 @@
+// engram_internal.cuh -- launch parameters and launchers shared by the kernel
+// translation units and the C ABI layer of libengram.  Not installed; the public
+// interface is include/engram.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engram.h"
+
+namespace engram {
+
+constexpr int kMaxHeads = ENGRAM_MAX_HEADS;
+constexpr int kMaxRows = 3 * kMaxHeads;
+
+struct CompressParams {
+  const int32_t *token_ids;
+  int64_t n;
+  const int32_t *tid2eid;
+  int32_t vocab;
+  int32_t n_eids;
+  int32_t *eids_out;
+  int32_t *status;
+};
+
+struct HashParams {
+  const int32_t *eids;
+  const int32_t *history;
+  int32_t *history_out;
+  int32_t *row_ids;
+  int32_t *status;
+  int64_t T;
+  int32_t batch, seq, H;
+  int32_t tokens_per_block;  // tokens whose 3H outputs one block owns
+  int32_t history_inline;    // 1: seq == 1 and the block writes history_out itself
+  uint64_t rows[3];
+  uint64_t seed[3][kMaxHeads];
+};
+
+struct LookupParams {
+  const int32_t *row_ids;
+  const uint8_t *table[3];
+  const float *scale[3];
+  int64_t rows[3];
+  const uint16_t *x;  // streams in  [T, 4, D]
+  uint16_t *y;        // streams out [T, 4, D]
+  const float *alpha;
+  float *gate_out;
+  float *mem_out;
+  int32_t *status;
+  int64_t T;
+  int32_t H, D;
+  int32_t tpt;  // threads per token (16 columns each)
+  int32_t tpb;  // tokens per block
+  float eps, inv_R, inv_D, sqrt_D;
+};
+
+cudaError_t launch_compress(const CompressParams &p, cudaStream_t stream);
+cudaError_t launch_hash(const HashParams &p, cudaStream_t stream);
+cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream);
+
+// splitmix64 first output for state x (S. Vigna, public domain), used for the
+// per-(order, head) hash seeds on the host.
+uint64_t splitmix64(uint64_t x);
+
+}  // namespace engram

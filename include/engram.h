@@ -1,0 +1,184 @@
+/*
+ * engram.h -- C ABI of libengram, the GB300 (sm_103a) Engram hashed n-gram memory
+ * lookup.
+ *
+ * The Engram lookup, as the pages describe it (VeOmni PR "support
+ * DeepSeek-V4.1-Flash in SeedOmni", PR description and commit "n-gram memory
+ * lookup"; NeMo AutoModel page, DeepseekV41Block.forward; vLLM page,
+ * DeepseekV4Model.forward): token ids are compressed through a many-to-one
+ * tid2eid map; the 2-, 3- and 4-gram windows of compressed ids are hashed into
+ * row ids [batch, sequence, hash_heads]; the rows are gathered from three tables
+ * (FP8 e4m3fn with a per-row scale, dequantised on lookup, or BF16); and a gated
+ * memory is added into the four mHC residual streams [batch, sequence, 4, hidden]
+ * before the layer.  The pages leave the hash, the combine and the gate open; this
+ * library implements them as follows:
+ *   seed(n, j)  = splitmix64(n*16 + j)            (first output, state n*16+j)
+ *   h           = seed; for each id e of the window, oldest first:
+ *                 h = (h ^ e) * 0x9E3779B97F4A7C15 mod 2^64;  h ^= h >> 29
+ *   row(n, j)   = h mod rows_n                     (unsigned, full 64-bit h)
+ *   m           = mean of the 3H dequantised rows  (fp32 accumulation)
+ *   g           = sigmoid( <rmsnorm(stream0), rmsnorm(m)> / sqrt(D) ),
+ *                 rmsnorm(x) = x / sqrt(mean(x^2) + eps), no learned weight
+ *   out_s       = bf16_rne(stream_s + g * alpha_s * m),  s = 0..3
+ *
+ * Conventions for every call:
+ *  - Pointers named *_host are host memory; every other data pointer is device
+ *    memory on the current CUDA device.  All memory is owned and allocated by the
+ *    caller; the library allocates nothing and keeps no pointer after a call.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on it; the library never synchronises
+ *    except in engram_read_status.
+ *  - Host-side argument errors are returned synchronously, before any launch:
+ *    nothing is written.  engram_last_error() then describes the argument.
+ *  - Data errors found on the device (a token id outside the vocabulary, a map
+ *    value or id out of range, a row id outside its table) never trap: the
+ *    kernel OR-s an ENGRAM_FLAG_* bit into *status (optional device int32; may be
+ *    NULL) and leaves that element's outputs unwritten.  Read the word with
+ *    engram_read_status or any device-to-host copy.
+ *  - bf16 values travel as their uint16 bit patterns.
+ *  - Requires a compute-capability 10.3 device (GB300); others get
+ *    ENGRAM_ERR_UNSUPPORTED.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ENGRAM_API __attribute__((visibility("default")))
+#else
+#define ENGRAM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t engram_status;
+
+#define ENGRAM_OK 0
+#define ENGRAM_ERR_INVALID_ARG 1  /* null, size, alignment, aliasing, range of an argument */
+#define ENGRAM_ERR_UNSUPPORTED 2  /* device is not sm_103, or a size beyond the limits below */
+#define ENGRAM_ERR_CUDA 3         /* a CUDA runtime call or kernel launch failed */
+#define ENGRAM_ERR_OUT_OF_RANGE 4 /* engram_read_status: a data range flag was set */
+#define ENGRAM_ERR_TIMEOUT 5      /* engram_read_status: a bounded device wait gave up */
+
+/* Bits of the device status word. */
+#define ENGRAM_FLAG_BAD_TOKEN 1 /* token id outside [0, vocab) */
+#define ENGRAM_FLAG_BAD_EID 2   /* tid2eid value outside [0, n_eids], or a negative id */
+#define ENGRAM_FLAG_BAD_ROW 4   /* row id outside [0, rows_n) */
+#define ENGRAM_FLAG_TIMEOUT 8   /* a bounded wait inside a kernel gave up */
+
+#define ENGRAM_MAX_HEADS 32   /* hash heads per n-gram order */
+#define ENGRAM_MAX_D 4096     /* row width = hidden size; D % 16 == 0 */
+
+#define ENGRAM_TABLE_FP8_E4M3FN 0
+#define ENGRAM_TABLE_BF16 1
+
+/*
+ * The three n-gram tables (index 0, 1, 2 = orders 2, 3, 4), row-major
+ * [rows[n], D], each 16-byte aligned.  FP8: one byte per element (OCP E4M3,
+ * "fn": bias 7, max 448, no infinities) and scale[n] = fp32 [rows[n]], the
+ * row's dequantisation factor (VeOmni PR page: FP8 tables with row-wise
+ * dequantisation on lookup).  BF16: two bytes per element, scale[n] ignored.
+ * 1 <= rows[n] <= 2^31 - 1.  The struct itself is read on the host during the
+ * call only.
+ */
+typedef struct engram_tables {
+  int32_t dtype; /* ENGRAM_TABLE_FP8_E4M3FN or ENGRAM_TABLE_BF16 */
+  int32_t D;     /* row width, multiple of 16, 16..ENGRAM_MAX_D */
+  int64_t rows[3];
+  const void *table[3];
+  const float *scale[3];
+} engram_tables;
+
+/*
+ * engram_compress -- tid2eid canonical token compression (VeOmni PR page, PR
+ * description and commit "n-gram memory lookup": a persistent many-to-one
+ * token_map baked at conversion time; the pad id 0 is what an unhashable
+ * position compresses to).
+ *   eids_out[i] = tid2eid[token_ids[i]],  i < n_tokens
+ * token_ids, eids_out: int32 [n_tokens] (may alias each other: in place is
+ * allowed); tid2eid: int32 [vocab], values expected in [0, n_eids].
+ * A token outside [0, vocab) sets ENGRAM_FLAG_BAD_TOKEN, a map value outside
+ * [0, n_eids] sets ENGRAM_FLAG_BAD_EID; that eids_out[i] is not written.
+ * n_tokens == 0 launches nothing and returns ENGRAM_OK.
+ */
+ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tokens,
+                                         const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
+                                         int32_t *eids_out, int32_t *status, void *stream);
+
+/*
+ * engram_hash -- n-gram hash ids per order and head (VeOmni PR page, commit
+ * "n-gram memory lookup" and the commit on the incremental decode cache: a
+ * window never reaches past position 0; a three-id tail of history is the whole
+ * cache and is exact; NeMo AutoModel page: engram_hash_ids [batch, sequence,
+ * hash_heads]).
+ *   eids        int32 [batch, seq] compressed ids (>= 0)
+ *   history     int32 [batch, 3] or NULL: the three ids before position 0,
+ *               oldest first; NULL means every sequence starts here (positions
+ *               before 0 are the pad id 0)
+ *   history_out int32 [batch, 3] or NULL: receives the last three ids of
+ *               history ++ eids, oldest first (the next call's history).  It
+ *               may be the same buffer as history; it must not overlap eids or
+ *               row_ids_out.
+ *   rows_host   host int64 [3]: rows of the 2-, 3-, 4-gram tables, 1..2^31-1
+ *   row_ids_out int32 [batch, seq, 3, n_heads], n-major: the row for order n,
+ *               head j of token (b, s) is at ((b*seq + s)*3 + n-2)*n_heads + j
+ * The window of order n at (b, s) is ids s-n+1 .. s.  A negative id in
+ * positions s-3 .. s sets ENGRAM_FLAG_BAD_EID and leaves that token's 3*n_heads
+ * ids unwritten.  1 <= n_heads <= ENGRAM_MAX_HEADS.
+ */
+ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,
+                                     const int32_t *history, int32_t *history_out,
+                                     int32_t n_heads, const int64_t *rows_host,
+                                     int32_t *row_ids_out, int32_t *status, void *stream);
+
+/*
+ * engram_lookup_fused -- gather + dequantise the 3*n_heads rows of every token,
+ * average them into m, gate with g = sigmoid(<rmsnorm(stream0), rmsnorm(m)> /
+ * sqrt(D)) and add g * alpha_s * m into the four mHC streams (VeOmni PR page:
+ * FP8 row-wise dequantisation on lookup, the Engram write goes into the streams
+ * before its layer; NeMo AutoModel page: streams [batch, sequence, streams,
+ * hidden]).  One pass over HBM: rows, stream 0..3 in, stream 0..3 out.
+ *   row_ids     int32 [n_tokens, 3*n_heads] as written by engram_hash
+ *   tables_host host struct describing the device tables (above)
+ *   streams_in  bf16 bits [n_tokens, 4, D], 16-byte aligned
+ *   streams_out bf16 bits [n_tokens, 4, D], 16-byte aligned; either exactly
+ *               streams_in (in place) or not overlapping it
+ *   alpha       fp32 [4] device: per-stream scale of the memory
+ *   eps         RMSNorm epsilon, finite, >= 0
+ *   gate_out    fp32 [n_tokens] or NULL: g per token
+ *   mem_out     fp32 [n_tokens, D] or NULL (16-byte aligned): m per token
+ * A row id outside its table sets ENGRAM_FLAG_BAD_ROW and leaves the token's
+ * outputs unwritten.
+ */
+ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
+                                             int32_t n_heads, const engram_tables *tables_host,
+                                             const uint16_t *streams_in, uint16_t *streams_out,
+                                             const float *alpha, float eps, float *gate_out,
+                                             float *mem_out, int32_t *status, void *stream);
+
+/*
+ * engram_read_status -- waits for `stream`, copies the device status word into
+ * *flags_host and returns ENGRAM_OK (no flag), ENGRAM_ERR_TIMEOUT
+ * (ENGRAM_FLAG_TIMEOUT set) or ENGRAM_ERR_OUT_OF_RANGE (a range flag set).  The
+ * word is not cleared.
+ */
+ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flags_host,
+                                            void *stream);
+
+/* Static, human-readable name of a status code. */
+ENGRAM_API const char *engram_status_string(engram_status code);
+
+/* Description of the last failed call on this host thread ("" if none). */
+ENGRAM_API const char *engram_last_error(void);
+
+/* ABI version of this header (incremented on any incompatible change). */
+#define ENGRAM_ABI_VERSION 1
+ENGRAM_API int32_t engram_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ENGRAM_H */

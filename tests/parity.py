@@ -1,0 +1,145 @@
+"""Shared pieces of the GPU parity tests: run a workload through the C ABI and
+through the CPU oracle on the same seeded inputs, and compare.
+
+Tolerances (the streams are bf16 outputs of fp32 arithmetic):
+* compressed ids, row ids, history: bit-exact;
+* streams: |y - y_ref| <= 2e-2 + 1e-2 |y_ref| elementwise (the stated max-abs
+  2e-2 / rel 1e-2 bar, read as an allclose), and in addition no element more
+  than one bf16 ulp from the oracle's once-rounded value, and at most 0.1% of
+  elements not bit-identical (the fp32 path rounds twice: fp32, then bf16);
+* m (fp32, sum of 3H products): within 1e-5 relative + 1e-6 of max |m|;
+* g (fp32 sigmoid of a 4096-term fp32 reduction): within 1e-5 absolute.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle
+import workloads as W
+
+STREAM_ATOL, STREAM_RTOL = 2e-2, 1e-2
+MAX_MISMATCH_FRAC = 1e-3
+
+
+@dataclasses.dataclass
+class HostInputs:
+    cfg: W.EngramConfig
+    ids: np.ndarray
+    tid2eid: np.ndarray
+    history: np.ndarray | None
+    tables: list
+    scales: list
+    streams: np.ndarray
+    alpha: np.ndarray
+
+
+def host_inputs(cfg: W.EngramConfig, rank: int = 0) -> HostInputs:
+    tabs, scales = W.tables_host(cfg)
+    return HostInputs(cfg, W.token_ids(cfg, rank), W.tid2eid(cfg), W.history(cfg, rank), tabs,
+                      scales, W.streams_host(cfg, rank), W.alpha(cfg))
+
+
+def oracle_path(inp: HostInputs):
+    cfg = inp.cfg
+    eids, f1 = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
+    rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history, want_history=True)
+    y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H,
+                                oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16, inp.tables,
+                                inp.scales, inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha,
+                                cfg.eps, aux=True)
+    return dict(eids=eids, rows=rows, history=hist, streams=y.reshape(inp.streams.shape), gate=g,
+                mem=m, flags=f1 | f2 | f3)
+
+
+def to_device(inp: HostInputs, device="cuda"):
+    import torch
+    import hashed_gram_memory_gb300 as eg
+    cfg = inp.cfg
+    dev = dict(
+        ids=torch.from_numpy(inp.ids).to(device),
+        tid2eid=torch.from_numpy(inp.tid2eid).to(device),
+        history=None if inp.history is None else torch.from_numpy(inp.history).to(device),
+        streams=torch.from_numpy(inp.streams.view(np.int16)).to(device),
+        alpha=torch.from_numpy(inp.alpha).to(device),
+    )
+    if cfg.dtype == W.FP8:
+        tabs = [torch.from_numpy(t).to(device) for t in inp.tables]
+        scs = [torch.from_numpy(s).to(device) for s in inp.scales]
+        dev["tables"] = eg.Tables(eg.TABLE_FP8_E4M3FN, tabs, scs)
+    else:
+        tabs = [torch.from_numpy(t.view(np.int16)).to(device) for t in inp.tables]
+        dev["tables"] = eg.Tables(eg.TABLE_BF16, tabs, None)
+    return dev
+
+
+def gpu_path(cfg: W.EngramConfig, dev: dict, aux: bool = True, in_place: bool = False):
+    """compress -> hash -> fused lookup through the C ABI; returns host arrays."""
+    import torch
+    import hashed_gram_memory_gb300 as eg
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eids = eg.engram_compress(dev["ids"], dev["tid2eid"], cfg.n_eids, status=status)
+    hist_out = None
+    if dev["history"] is not None:
+        hist_out = torch.empty_like(dev["history"])
+    rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=dev["history"], history_out=hist_out,
+                          status=status)
+    gate = torch.full((cfg.T,), float("nan"), device="cuda") if aux else None
+    mem = torch.full((cfg.T, cfg.D), float("nan"), device="cuda") if aux else None
+    x = dev["streams"]
+    out = x.clone() if in_place else torch.empty_like(x)
+    src = out if in_place else x
+    eg.engram_lookup_fused(rows, cfg.H, dev["tables"], src, dev["alpha"], cfg.eps, streams_out=out,
+                           gate_out=gate, mem_out=mem, status=status)
+    code, flags = eg.engram_read_status(status)
+    res = dict(eids=eids.cpu().numpy(), rows=rows.cpu().numpy(),
+               history=None if hist_out is None else hist_out.cpu().numpy(),
+               streams=out.cpu().numpy().view(np.uint16), flags=flags, code=code)
+    if aux:
+        res["gate"] = gate.cpu().numpy()
+        res["mem"] = mem.cpu().numpy()
+    return res
+
+
+def bf16_ulp(y: np.ndarray) -> np.ndarray:
+    a = np.abs(y.astype(np.float64))
+    e = np.frexp(np.maximum(a, 2.0 ** -126))[1]
+    return np.ldexp(1.0, e - 8)
+
+
+def compare_streams(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str = "streams"):
+    yg = oracle.bf16_bits_to_float(y_gpu_bits).astype(np.float64)
+    yr = oracle.bf16_bits_to_float(y_ref_bits).astype(np.float64)
+    assert np.isfinite(yg).all(), f"{what}: non-finite output"
+    err = np.abs(yg - yr)
+    bound = STREAM_ATOL + STREAM_RTOL * np.abs(yr)
+    worst = float(np.max(err / bound)) if err.size else 0.0
+    assert np.all(err <= bound), f"{what}: allclose bar exceeded, worst err/bound {worst:.3g}"
+    ulp = bf16_ulp(yr)
+    assert np.all(err <= ulp * 1.0000001), f"{what}: max err {np.max(err / ulp):.3g} ulp"
+    mism = float(np.mean(y_gpu_bits != y_ref_bits)) if err.size else 0.0
+    assert mism <= MAX_MISMATCH_FRAC, f"{what}: {mism:.2e} of elements not bit-identical"
+    return dict(max_abs=float(err.max()) if err.size else 0.0, mismatch_frac=mism)
+
+
+def compare_mem(m_gpu, m_ref):
+    scale = float(np.max(np.abs(m_ref))) if m_ref.size else 0.0
+    np.testing.assert_allclose(m_gpu, m_ref, rtol=1e-5, atol=1e-6 * scale + 1e-30)
+
+
+def compare_gate(g_gpu, g_ref):
+    np.testing.assert_allclose(g_gpu, g_ref, rtol=0, atol=1e-5)
+
+
+def compare_all(res: dict, ref: dict, aux: bool = True):
+    assert res["flags"] == ref["flags"] == 0, (res["flags"], ref["flags"])
+    assert np.array_equal(res["eids"], ref["eids"])
+    assert np.array_equal(res["rows"], ref["rows"])
+    if ref["history"] is not None and res["history"] is not None:
+        assert np.array_equal(res["history"], ref["history"])
+    stats = compare_streams(res["streams"], ref["streams"])
+    if aux:
+        compare_mem(res["mem"], ref["mem"])
+        compare_gate(res["gate"], ref["gate"])
+    return stats

@@ -1,0 +1,124 @@
+"""The C ABI on the host, without a GPU: the library loads, exports every entry
+point include/engram.h declares (and no other engram_ symbol), and argument
+errors come back synchronously as ENGRAM_ERR_INVALID_ARG / UNSUPPORTED before
+anything touches a device."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "engram.h")
+
+
+@pytest.fixture(scope="module")
+def eg():
+    from hashed_gram_memory_gb300 import build
+    build.build()
+    import hashed_gram_memory_gb300 as eg
+    return eg
+
+
+def declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"ENGRAM_API\s+[\w\s\*]+?\b(engram_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("engram_compress", "engram_hash", "engram_lookup_fused", "engram_read_status",
+              "engram_status_string", "engram_last_error", "engram_abi_version"):
+        assert n in names
+
+
+def test_header_is_plain_c():
+    src = open(HEADER).read()
+    assert "torch" not in src and "cuda_runtime" not in src and "<c10" not in src
+    r = subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-x", "c", HEADER], capture_output=True,
+                       text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_library_exports_every_declared_symbol(eg):
+    for n in declared():
+        assert hasattr(eg.lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", eg.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted({ln.split()[-1] for ln in out.splitlines() if " T engram_" in ln})
+    assert exported == declared()
+
+
+def test_abi_version_and_strings(eg):
+    assert eg.engram_abi_version() == 1
+    for code in range(6):
+        assert eg.engram_status_string(code).startswith("ENGRAM")
+    assert "unknown" in eg.engram_status_string(99)
+
+
+def _tables(dtype=0, D=64, rows=(10, 10, 10), ptr=0x10000, scale=0x20000):
+    import hashed_gram_memory_gb300 as eg
+    s = eg.engram_tables()
+    s.dtype, s.D = dtype, D
+    for n in range(3):
+        s.rows[n] = rows[n]
+        s.table[n] = ptr + n * 0x100000
+        s.scale[n] = scale + n * 0x1000 if scale else None
+    return s
+
+
+def test_host_argument_errors(eg):
+    L = eg.lib
+    INV, UNS = eg.ERR_INVALID_ARG, eg.ERR_UNSUPPORTED
+    rows = (C.c_int64 * 3)(5, 5, 5)
+    bad_rows = (C.c_int64 * 3)(5, 0, 5)
+    p = C.c_void_p(0x1000)
+    assert L.engram_compress(p, -1, p, 10, 5, p, None, None) == INV
+    assert L.engram_compress(p, 4, None, 10, 5, p, None, None) == INV
+    assert L.engram_compress(p, 4, p, 0, 5, p, None, None) == INV
+    assert L.engram_compress(C.c_void_p(0x1002), 4, p, 10, 5, C.c_void_p(0x2000), None, None) == INV
+    assert L.engram_compress(C.c_void_p(0x1000), 4, p, 10, 5, C.c_void_p(0x1004), None, None) == INV
+    assert b"partially" in L.engram_last_error()
+    assert L.engram_hash(p, 2, 3, None, None, 0, rows, C.c_void_p(0x9000), None, None) == INV
+    assert L.engram_hash(p, 2, 3, None, None, 33, rows, C.c_void_p(0x9000), None, None) == INV
+    assert L.engram_hash(p, 2, 3, None, None, 2, bad_rows, C.c_void_p(0x9000), None, None) == INV
+    assert L.engram_hash(p, -1, 3, None, None, 2, rows, C.c_void_p(0x9000), None, None) == INV
+    assert L.engram_hash(p, 2, 3, None, None, 2, rows, C.c_void_p(0x1008), None, None) == INV
+    # history and history_out may be the same buffer, but not partially overlap
+    assert L.engram_hash(p, 2, 3, C.c_void_p(0x5000), C.c_void_p(0x5004), 2, rows,
+                         C.c_void_p(0x9000), None, None) == INV
+    # empty work returns OK without a launch or a device query
+    assert L.engram_hash(None, 0, 3, None, None, 2, rows, None, None, None) == eg.OK
+    assert L.engram_compress(None, 0, p, 10, 5, None, None, None) == eg.OK
+
+    x, y, a, ids = C.c_void_p(0x100000000), C.c_void_p(0x200000000), C.c_void_p(0x3000), C.c_void_p(0x4000)
+    t = _tables()
+    assert L.engram_lookup_fused(ids, 8, 0, C.byref(t), x, y, a, 1e-6, None, None, None, None) == INV
+    assert L.engram_lookup_fused(ids, 8, 2, None, x, y, a, 1e-6, None, None, None, None) == INV
+    for bad in (_tables(D=40), _tables(D=0), _tables(dtype=7), _tables(rows=(10, 0, 10)),
+                _tables(ptr=0x10008), _tables(scale=0)):
+        assert L.engram_lookup_fused(ids, 8, 2, C.byref(bad), x, y, a, 1e-6, None, None, None,
+                                     None) == INV
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(_tables(D=8192)), x, y, a, 1e-6, None, None,
+                                 None, None) == UNS
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(t), x, y, a, -1.0, None, None, None, None) == INV
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(t), x, y, a, float("nan"), None, None, None,
+                                 None) == INV
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(t), x, y, None, 1e-6, None, None, None,
+                                 None) == INV
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(t), C.c_void_p(0x100000008), y, a, 1e-6, None,
+                                 None, None, None) == INV
+    # streams_out overlapping streams_in without being equal
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(t), x, C.c_void_p(0x100000010), a, 1e-6, None,
+                                 None, None, None) == INV
+    # BF16 tables do not need scales
+    tb = _tables(dtype=1, scale=0)
+    assert L.engram_lookup_fused(ids, 0, 2, C.byref(tb), None, None, a, 1e-6, None, None, None,
+                                 None) == eg.OK
+
+
+def test_python_binding_rejects_cpu_tensors(eg):
+    import torch
+    with pytest.raises(eg.EngramError):
+        eg.engram_compress(torch.zeros(4, dtype=torch.int32), torch.zeros(4, dtype=torch.int32), 3)

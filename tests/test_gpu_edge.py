@@ -1,0 +1,149 @@
+"""GPU edge cases through the C ABI: empty inputs, device-detected bad ids (status
+flags, the affected outputs left unwritten, every other output still exact),
+decode steps with the history updated in place against the prefill, and the
+zero-gate invariants."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eg():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hashed_gram_memory_gb300 as eg
+    return eg
+
+
+def _t(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_empty_inputs(eg):
+    import torch
+    cfg = W.CONFIGS[0].scaled(S=0)
+    inp = P.host_inputs(W.CONFIGS[0])
+    dev = P.to_device(inp)
+    e = eg.engram_compress(torch.zeros((1, 0), dtype=torch.int32, device="cuda"), dev["tid2eid"], 800)
+    assert e.numel() == 0
+    r = eg.engram_hash(e, 2, cfg.rows)
+    assert r.shape == (1, 0, 3, 2)
+    y = eg.engram_lookup_fused(r, 2, dev["tables"], torch.empty((0, 4, 256), dtype=torch.int16,
+                                                                device="cuda"), dev["alpha"])
+    assert y.numel() == 0
+    # seq == 0 with a history: history_out is the history itself
+    h = _t(np.array([[4, 5, 6], [7, 8, 9]], np.int32))
+    ho = torch.full_like(h, -1)
+    eg.engram_hash(torch.zeros((2, 0), dtype=torch.int32, device="cuda"), 2, cfg.rows, history=h,
+                   history_out=ho)
+    assert ho.cpu().tolist() == [[4, 5, 6], [7, 8, 9]]
+    torch.cuda.synchronize()
+
+
+def test_compress_flags_and_unwritten(eg):
+    import torch
+    m = np.array([3, 0, 9, 12, 5], np.int32)          # 12 > n_eids = 10
+    ids = np.array([0, 1, 2, 3, 4, 5, -1, 2], np.int32)
+    ref, rflags = oracle.compress(ids, m, 10, fill=-7)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((8,), -7, dtype=torch.int32, device="cuda")
+    eg.engram_compress(_t(ids), _t(m), 10, eids_out=out, status=st)
+    code, flags = eg.engram_read_status(st)
+    assert code == eg.ERR_OUT_OF_RANGE and flags == rflags == (eg.FLAG_BAD_TOKEN | eg.FLAG_BAD_EID)
+    assert out.cpu().numpy().tolist() == ref.tolist()
+
+
+def test_hash_flags_negative_ids_and_unwritten(eg):
+    import torch
+    eids = np.array([[3, 4, -1, 5, 6, 7, 8, 9], [1, 2, 3, 4, 5, 6, 7, 8]], np.int32)
+    hist = np.array([[1, 2, 3], [-4, 5, 6]], np.int32)
+    rows = (101, 103, 107)
+    ref, rflags = oracle.hash_ids(eids, 2, rows, history=hist, fill=-7)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((2, 8, 3, 2), -7, dtype=torch.int32, device="cuda")
+    eg.engram_hash(_t(eids), 2, rows, history=_t(hist), row_ids_out=out, status=st)
+    code, flags = eg.engram_read_status(st)
+    assert flags == rflags == eg.FLAG_BAD_EID
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_lookup_flags_bad_rows_and_leaves_token_unwritten(eg):
+    import torch
+    cfg = W.CONFIGS[0].scaled(S=37)
+    inp = P.host_inputs(cfg)
+    eids, _ = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
+    rows, _ = oracle.hash_ids(eids, cfg.H, cfg.rows)
+    rows = rows.reshape(cfg.T, -1).copy()
+    rows[3, 1] = cfg.rows[0]          # one past the end of the 2-gram table
+    rows[20, 5] = -2
+    ref, _, _, rflags = oracle.lookup(rows, cfg.H, oracle.FP8, inp.tables, inp.scales,
+                                      inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha, cfg.eps,
+                                      aux=True, fill=0x1234)
+    dev = P.to_device(inp)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((cfg.T, 4, cfg.D), 0x1234, dtype=torch.int16, device="cuda")
+    eg.engram_lookup_fused(_t(rows), cfg.H, dev["tables"], dev["streams"].view(cfg.T, 4, cfg.D),
+                           dev["alpha"], cfg.eps, streams_out=out, status=st)
+    code, flags = eg.engram_read_status(st)
+    assert code == eg.ERR_OUT_OF_RANGE and flags == rflags == eg.FLAG_BAD_ROW
+    got = out.cpu().numpy().view(np.uint16)
+    assert (got[3] == 0x1234).all() and (got[20] == 0x1234).all()
+    keep = [t for t in range(cfg.T) if t not in (3, 20)]
+    P.compare_streams(got[keep], ref[keep])
+
+
+@pytest.mark.parametrize("split", [0, 1, 2, 3, 9])
+def test_decode_steps_in_place_history_equal_prefill(eg, split):
+    import torch
+    cfg = W.CONFIGS[2].scaled(B=5, S=1, rows=(5_040_000,) * 3)
+    g = np.random.default_rng(17 + split)
+    S = 14
+    eids = g.integers(1, 100_000, size=(cfg.B, S)).astype(np.int32)
+    full = eg.engram_hash(_t(eids), cfg.H, cfg.rows).cpu().numpy()
+    ref, _ = oracle.hash_ids(eids, cfg.H, cfg.rows)
+    assert np.array_equal(full, ref)
+    hist = torch.empty((cfg.B, 3), dtype=torch.int32, device="cuda")
+    parts = [eg.engram_hash(_t(eids[:, :split]), cfg.H, cfg.rows, history_out=hist).cpu().numpy()]
+    for s in range(split, S):
+        # history and history_out are the same buffer: the decode cache updated in place
+        parts.append(eg.engram_hash(_t(eids[:, s:s + 1]), cfg.H, cfg.rows, history=hist,
+                                    history_out=hist).cpu().numpy())
+    assert np.array_equal(np.concatenate(parts, axis=1), full)
+    assert np.array_equal(hist.cpu().numpy(), eids[:, -3:])
+
+
+def test_two_token_step_in_place_history(eg):
+    import torch
+    hist0 = np.array([[5, 6, 7], [1, 2, 3]], np.int32)
+    eids = np.array([[9, 10], [11, 12]], np.int32)
+    rows = (1009, 1013, 1019)
+    ref, href, _ = oracle.hash_ids(eids, 3, rows, history=hist0, want_history=True)
+    h = _t(hist0)
+    got = eg.engram_hash(_t(eids), 3, rows, history=h, history_out=h).cpu().numpy()
+    assert np.array_equal(got, ref) and np.array_equal(h.cpu().numpy(), href)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("dtype", [W.FP8, W.BF16])
+def test_zero_alpha_and_zero_rows_leave_streams_bit_identical(eg, dtype):
+    import torch
+    base = W.CONFIGS[0] if dtype == W.FP8 else W.CONFIGS[4].scaled(B=1, S=64, rows=(97, 89, 83))
+    inp = P.host_inputs(base)
+    assert not (inp.streams == 0x8000).any()
+    dev = P.to_device(inp)
+    dev["alpha"] = torch.zeros(4, dtype=torch.float32, device="cuda")
+    res = P.gpu_path(base, dev, aux=False)
+    assert np.array_equal(res["streams"], inp.streams)
+    dev = P.to_device(inp)
+    for t in dev["tables"].tables:
+        t.zero_()
+    res = P.gpu_path(base, dev, aux=True)
+    assert np.array_equal(res["streams"], inp.streams)
+    assert np.all(res["mem"] == 0) and np.allclose(res["gate"], 0.5)

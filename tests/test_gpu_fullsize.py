@@ -1,0 +1,102 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark
+times (no aux outputs, out-of-place streams): tables and streams are generated on
+the GPU, token ids on the host.  Every compressed id and every row id is checked
+against the oracle; the streams are checked on a seeded sample of tokens, for
+which the oracle gets exactly the table rows and stream values the GPU read
+(copied back from the device: inputs, not results)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE = 192
+
+
+@pytest.fixture(scope="module")
+def eg():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hashed_gram_memory_gb300 as eg
+    return eg
+
+
+def run_full(eg, cfg, device_inputs):
+    """compress -> hash -> lookup exactly as bench.py launches them."""
+    import torch
+    d = device_inputs
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eids = eg.engram_compress(d["ids"], d["tid2eid"], cfg.n_eids, status=st)
+    hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
+    rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=d["history"], history_out=hist_out,
+                          status=st)
+    out = torch.empty_like(d["streams"])
+    eg.engram_lookup_fused(rows, cfg.H, d["tables"], d["streams"], d["alpha"], cfg.eps,
+                           streams_out=out, status=st)
+    code, flags = eg.engram_read_status(st)
+    return eids, rows, hist_out, out, flags
+
+
+def device_inputs(eg, cfg):
+    import torch
+    tabs, scales = W.tables_device(cfg, "cuda")
+    dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
+    hist = W.history(cfg)
+    return dict(ids=torch.from_numpy(W.token_ids(cfg)).cuda(),
+                tid2eid=torch.from_numpy(W.tid2eid(cfg)).cuda(),
+                history=None if hist is None else torch.from_numpy(hist).cuda(),
+                streams=W.streams_device(cfg, "cuda"),
+                alpha=torch.from_numpy(W.alpha(cfg)).cuda(),
+                tables=eg.Tables(dt, tabs, scales))
+
+
+@pytest.mark.parametrize("ci", [1, 2, 3, 4])
+def test_full_size_sampled(eg, ci):
+    import torch
+    cfg = W.CONFIGS[ci]
+    free = torch.cuda.mem_get_info()[0]
+    need = cfg.table_bytes() + 2 * cfg.T * 4 * cfg.D * 2 + (4 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.1f} GiB of device memory, {free / 2**30:.1f} free")
+    d = device_inputs(eg, cfg)
+    eids, rows, hist_out, out, flags = run_full(eg, cfg, d)
+    assert flags == 0
+
+    # every index, bit-exact
+    ids_h = d["ids"].cpu().numpy()
+    e_ref, f1 = oracle.compress(ids_h, d["tid2eid"].cpu().numpy(), cfg.n_eids)
+    hist_h = None if d["history"] is None else d["history"].cpu().numpy()
+    r_ref, h_ref, f2 = oracle.hash_ids(e_ref, cfg.H, cfg.rows, history=hist_h, want_history=True)
+    assert f1 == f2 == 0
+    assert np.array_equal(eids.cpu().numpy(), e_ref)
+    assert np.array_equal(rows.cpu().numpy(), r_ref)
+    if hist_out is not None:
+        assert np.array_equal(hist_out.cpu().numpy(), h_ref)
+
+    # streams on a seeded sample of tokens (first, last, random)
+    g = np.random.default_rng(1000 + ci)
+    T = cfg.T
+    toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(N_SAMPLE, T), replace=False)]))
+    rr = r_ref.reshape(T, -1)[toks]                       # [K, 3H]
+    tabs, scs, remap = [], [], np.empty_like(rr)
+    for n in range(3):
+        cols = slice(n * cfg.H, (n + 1) * cfg.H)
+        uniq, inv = np.unique(rr[:, cols], return_inverse=True)
+        remap[:, cols] = inv.reshape(rr[:, cols].shape)
+        idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
+        t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
+        tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))
+        scs.append(d["tables"].scales[n].index_select(0, idx).cpu().numpy()
+                   if cfg.dtype == W.FP8 else None)
+    x = d["streams"].view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
+    y_ref, f3 = oracle.lookup(remap, cfg.H, oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16, tabs,
+                              scs, x, d["alpha"].cpu().numpy(), cfg.eps)
+    assert f3 == 0
+    y = out.view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
+    P.compare_streams(y, y_ref, what=f"{cfg.name} sampled streams")
+    del d, out, rows, eids
+    torch.cuda.empty_cache()

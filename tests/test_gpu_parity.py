@@ -1,0 +1,60 @@
+"""GPU parity: the C ABI against the CPU oracle, element by element, on the same
+seeded inputs at sizes the oracle finishes in seconds (several blocks and a
+ragged tail), for every workload shape plus stress cases: a loud memory (row
+scales near 1, so an error in m shows in the streams), odd row widths, one and
+the maximum number of heads, one-row tables, in-place streams."""
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+C = W.CONFIGS
+SMALL = {
+    "tiny_fp8_d256": C[0],
+    "mid_prefill_fp8": C[1].scaled(B=2, S=301, rows=(4099, 5003, 6007)),
+    "decode_fp8": C[2].scaled(B=300, rows=(7001, 7013, 7019)),
+    "full_prefill_fp8": C[3].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "bf16_tables": C[4].scaled(B=3, S=133, rows=(3001, 3011, 3019)),
+    "loud_fp8": C[3].scaled(B=1, S=211, rows=(1009, 1013, 1019), scale_lo=0.5, scale_hi=1.0),
+    "loud_bf16": C[4].scaled(B=1, S=199, rows=(1009, 1013, 1019), bf16_std=1.0),
+    "d48_h1": C[0].scaled(S=97, D=48, H=1, rows=(11, 13, 17)),
+    "d1040_h5": C[1].scaled(B=1, S=77, D=1040, H=5, rows=(101, 103, 107), scale_lo=0.5,
+                            scale_hi=1.0),
+    "d16_h32_bf16": C[4].scaled(B=2, S=41, D=16, H=32, rows=(1, 2, 3), bf16_std=1.0),
+    "d4096_h32": C[3].scaled(B=1, S=19, H=32, rows=(50, 60, 70)),
+    "d2560_decode": C[2].scaled(B=37, D=2560, rows=(97, 89, 83)),
+}
+
+
+@pytest.fixture(scope="module")
+def eg():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hashed_gram_memory_gb300 as eg
+    return eg
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_parity_vs_oracle(eg, name):
+    cfg = SMALL[name]
+    inp = P.host_inputs(cfg)
+    ref = P.oracle_path(inp)
+    res = P.gpu_path(cfg, P.to_device(inp), aux=True)
+    P.compare_all(res, ref)
+    # The production launch (no aux outputs) must give the same streams bit for bit.
+    res2 = P.gpu_path(cfg, P.to_device(inp), aux=False)
+    assert np.array_equal(res2["streams"], res["streams"])
+
+
+@pytest.mark.parametrize("name", ["tiny_fp8_d256", "bf16_tables", "d1040_h5"])
+def test_in_place_streams(eg, name):
+    cfg = SMALL[name]
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    a = P.gpu_path(cfg, dev, aux=False)
+    b = P.gpu_path(cfg, dev, aux=False, in_place=True)
+    assert np.array_equal(a["streams"], b["streams"])
