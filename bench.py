@@ -51,11 +51,20 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch (small cases for ncu captures)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the rows of each table (small cases for ncu captures)")
     return ap.parse_args()
 
 
-def config_of(name: str) -> W.EngramConfig:
-    return next(c for c in W.CONFIGS if c.name == name)
+def config_of(name: str, args=None) -> W.EngramConfig:
+    cfg = next(c for c in W.CONFIGS if c.name == name)
+    if args is not None and args.batch:
+        cfg = cfg.scaled(B=args.batch)
+    if args is not None and args.rows:
+        cfg = cfg.scaled(rows=(args.rows,) * 3)
+    return cfg
 
 
 def workload_desc(cfg: W.EngramConfig) -> dict:
@@ -206,6 +215,7 @@ def run_native(args):
     import torch
     import torch.distributed as dist
     import hashed_gram_memory_gb300 as eg
+    from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -217,7 +227,7 @@ def run_native(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
 
-    cfg = config_of(args.workload)
+    cfg = config_of(args.workload, args)
     d = device_inputs(eg, cfg, rank, device)
     stream = torch.cuda.Stream(device)
     step = Step(eg, cfg, d, stream)
@@ -251,10 +261,7 @@ def run_native(args):
         dist.barrier()
     ms_total = t_begin.elapsed_time(t_end)
     lookup_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, device)
     code, flags = eg.engram_read_status(step.status, stream)
     clk = clocks.summary(wall0, wall1) if clocks else None
     if clocks:
@@ -269,7 +276,7 @@ def run_native(args):
         lk = statistics.mean(lookup_ms)
         achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
         traffic = recorded_traffic(cfg)
-        value = world * cfg.T * K / (ms_total * 1e-3)
+        value = whole_job_throughput(world * cfg.T * K, ms_total * 1e-3)
         line = {
             "metric": METRIC,
             "value": value,
@@ -317,6 +324,7 @@ def run_e2e(eg, cfg, step, stream, steps, world, device):
     and copies the updated streams back, all inside the timed region."""
     import torch
     import torch.distributed as dist
+    from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
     d = step.d
     ids_h = d["ids"].cpu().pin_memory()
     x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
@@ -344,13 +352,10 @@ def run_e2e(eg, cfg, step, stream, steps, world, device):
             one()
     stream.synchronize()
     dt = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([dt], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        dt = float(tt.item())
+    dt = max_over_ranks(dt, device)
     h2d = ids_h.numel() * 4 + x_h.numel() * 2
     d2h = y_h.numel() * 2
-    return {"value": world * cfg.T * steps / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "how": "pinned host ids + streams -> device, compress/hash/lookup, streams -> host; "
                    "one CUDA stream, timed on the host around the steps"}
@@ -451,7 +456,7 @@ def run_reference(args, budget_s: float = 60.0):
     if rank != 0:
         return
     import oracle
-    cfg = config_of(args.workload)
+    cfg = config_of(args.workload, args)
     K = max(1, args.steps)
     probe = reference_sample(cfg, min(256, cfg.T))
     rate = probe["n"] / time_oracle(cfg, probe)

@@ -15,7 +15,11 @@ HEADER = os.path.join(ROOT, "include", "engram.h")
 
 @pytest.fixture(scope="module")
 def eg():
-    from hashed_gram_memory_gb300 import build
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_engram_build", os.path.join(ROOT, "hashed_gram_memory_gb300", "build.py"))
+    build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build)
     build.build()
     import hashed_gram_memory_gb300 as eg
     return eg
