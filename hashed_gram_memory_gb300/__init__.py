@@ -111,7 +111,8 @@ class Tables:
         for n in range(3):
             s.rows[n] = int(self.tables[n].shape[0])
             s.table[n] = self.tables[n].data_ptr()
-            s.scale[n] = self.scales[n].data_ptr() if self.scales else None
+            sc = self.scales[n] if self.scales else None
+            s.scale[n] = sc.data_ptr() if sc is not None else None
         return s
 
 

@@ -1,0 +1,82 @@
+// lookup_common.cuh -- device helpers shared by the two lookup kernels: the
+// dequantisation of 16 columns of a row, the bf16 unpack / pack, and the gate.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace engram {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// acc[0..16) += scale * e4m3(v[0..16)); e4m3 -> f16 -> f32 is exact.
+__device__ __forceinline__ void acc_fp8(float (&acc)[16], const uint4 &v, float scale) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2_raw lo =
+        __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    acc[4 * q + 0] = fmaf(a.x, scale, acc[4 * q + 0]);
+    acc[4 * q + 1] = fmaf(a.y, scale, acc[4 * q + 1]);
+    acc[4 * q + 2] = fmaf(b.x, scale, acc[4 * q + 2]);
+    acc[4 * q + 3] = fmaf(b.y, scale, acc[4 * q + 3]);
+  }
+}
+
+// acc[0..8) += bf16(v[0..8)).
+__device__ __forceinline__ void acc_bf16(float *acc, const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q + 0] += bf16_lo(w[q]);
+    acc[2 * q + 1] += bf16_hi(w[q]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Partial sums of the gate over 16 columns: sum a^2, sum m^2, sum a*m, with a =
+// stream 0 (two 16-byte words of bf16) and m the memory.
+__device__ __forceinline__ void gate_partials(const uint4 &a_lo, const uint4 &a_hi,
+                                              const float (&m)[16], float &saa, float &smm,
+                                              float &sam) {
+  const uint32_t a32[8] = {a_lo.x, a_lo.y, a_lo.z, a_lo.w, a_hi.x, a_hi.y, a_hi.z, a_hi.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float a0 = bf16_lo(a32[q]), a1 = bf16_hi(a32[q]);
+    const float m0 = m[2 * q], m1 = m[2 * q + 1];
+    saa = fmaf(a0, a0, fmaf(a1, a1, saa));
+    smm = fmaf(m0, m0, fmaf(m1, m1, smm));
+    sam = fmaf(a0, m0, fmaf(a1, m1, sam));
+  }
+}
+
+// g = sigmoid( sum(a m) / (rms(a) rms(m) sqrt(D)) ),  rms(x) = sqrt(mean(x^2) + eps).
+__device__ __forceinline__ float gate_value(float saa, float smm, float sam, float Df, float eps,
+                                            float sqrt_D) {
+  const float rms_a = sqrtf(saa / Df + eps);
+  const float rms_m = sqrtf(smm / Df + eps);
+  const float logit = sam / (rms_a * rms_m * sqrt_D);
+  return 1.f / (1.f + expf(-logit));
+}
+
+// out = bf16_rne(x + c * m) for 8 columns held as one 16-byte word of bf16.
+__device__ __forceinline__ uint4 gated_add8(const uint4 &in, const float *m, float c) {
+  uint4 out;
+  out.x = pack_bf16(fmaf(c, m[0], bf16_lo(in.x)), fmaf(c, m[1], bf16_hi(in.x)));
+  out.y = pack_bf16(fmaf(c, m[2], bf16_lo(in.y)), fmaf(c, m[3], bf16_hi(in.y)));
+  out.z = pack_bf16(fmaf(c, m[4], bf16_lo(in.z)), fmaf(c, m[5], bf16_hi(in.z)));
+  out.w = pack_bf16(fmaf(c, m[6], bf16_lo(in.w)), fmaf(c, m[7], bf16_hi(in.w)));
+  return out;
+}
+
+}  // namespace engram

@@ -168,6 +168,40 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
 ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flags_host,
                                             void *stream);
 
+/*
+ * Kernel choice of engram_lookup_fused for this process:
+ *   ENGRAM_LOOKUP_AUTO    the library picks (default);
+ *   ENGRAM_LOOKUP_GATHER  register-direct gathers, one token per thread group
+ *                         (any D);
+ *   ENGRAM_LOOKUP_BULK    persistent kernel: one producer warp streams rows and
+ *                         streams into a shared-memory ring with 1-D bulk copies
+ *                         (TMA) under mbarriers; D % 512 == 0 only, otherwise the
+ *                         call falls back to GATHER.
+ * Both give identical results.  Returns the previous setting, or -1 for an
+ * unknown value (nothing changed).  Not synchronised with calls in flight on
+ * other host threads.
+ */
+#define ENGRAM_LOOKUP_AUTO 0
+#define ENGRAM_LOOKUP_GATHER 1
+#define ENGRAM_LOOKUP_BULK 2
+ENGRAM_API int32_t engram_set_lookup_kernel(int32_t which);
+
+/*
+ * Every wait inside a kernel on data another warp produces (an mbarrier phase)
+ * gives up after this many nanoseconds, sets ENGRAM_FLAG_TIMEOUT and ends the
+ * kernel early instead of hanging.  Default 250 ms; values below 1 ms are
+ * raised to 1 ms.  Returns the previous limit.
+ */
+ENGRAM_API int64_t engram_set_wait_limit_ns(int64_t ns);
+
+/*
+ * Test hook for the timeout path: the next `launches` launches of the BULK
+ * lookup kernel withhold one row copy in every block (the mbarrier still
+ * expects its bytes), so the consumers' bounded wait runs out and the launch
+ * reports ENGRAM_FLAG_TIMEOUT.  For tests only; 0 turns it off.
+ */
+ENGRAM_API void engram_debug_withhold_copies(int32_t launches);
+
 /* Static, human-readable name of a status code. */
 ENGRAM_API const char *engram_status_string(engram_status code);
 
