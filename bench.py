@@ -55,6 +55,7 @@ def parse():
                     help="override the batch (small cases for ncu captures)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the rows of each table (small cases for ncu captures)")
+    ap.add_argument("--lookup-kernel", default="auto", choices=["auto", "gather", "bulk"])
     return ap.parse_args()
 
 
@@ -228,6 +229,8 @@ def run_native(args):
         dist.init_process_group("nccl", device_id=device)
 
     cfg = config_of(args.workload, args)
+    eg.engram_set_lookup_kernel({"auto": eg.LOOKUP_AUTO, "gather": eg.LOOKUP_GATHER,
+                                 "bulk": eg.LOOKUP_BULK}[args.lookup_kernel])
     d = device_inputs(eg, cfg, rank, device)
     stream = torch.cuda.Stream(device)
     step = Step(eg, cfg, d, stream)
@@ -294,6 +297,7 @@ def run_native(args):
             "hbm_gbs_effective_step": bytes_tok * cfg.T * K / (ms_total * 1e-3) / 1e9,
             "roofline": {
                 "kernel": "engram_lookup_fused",
+                "lookup_kernel": args.lookup_kernel,
                 "bound": "hbm",
                 "achieved": achieved,
                 "peak": peak,

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libengram.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_TIMEOUT = range(6)
 FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
 TABLE_FP8_E4M3FN, TABLE_BF16 = 0, 1
+LOOKUP_AUTO, LOOKUP_GATHER, LOOKUP_BULK = 0, 1, 2
 MAX_HEADS, MAX_D = 32, 4096
 
 
@@ -52,6 +53,12 @@ def _load():
     L.engram_last_error.argtypes = []
     L.engram_last_error.restype = C.c_char_p
     L.engram_abi_version.restype = C.c_int32
+    L.engram_set_lookup_kernel.argtypes = [C.c_int32]
+    L.engram_set_lookup_kernel.restype = C.c_int32
+    L.engram_set_wait_limit_ns.argtypes = [C.c_int64]
+    L.engram_set_wait_limit_ns.restype = C.c_int64
+    L.engram_debug_withhold_copies.argtypes = [C.c_int32]
+    L.engram_debug_withhold_copies.restype = None
     return L
 
 
@@ -192,3 +199,19 @@ def engram_status_string(code: int) -> str:
 
 def engram_abi_version() -> int:
     return int(lib.engram_abi_version())
+
+
+def engram_set_lookup_kernel(which: int) -> int:
+    """LOOKUP_AUTO / LOOKUP_GATHER / LOOKUP_BULK for this process; returns the previous one."""
+    prev = int(lib.engram_set_lookup_kernel(which))
+    if prev < 0:
+        raise EngramError(ERR_INVALID_ARG, f"unknown lookup kernel {which}")
+    return prev
+
+
+def engram_set_wait_limit_ns(ns: int) -> int:
+    return int(lib.engram_set_wait_limit_ns(int(ns)))
+
+
+def engram_debug_withhold_copies(launches: int) -> None:
+    lib.engram_debug_withhold_copies(int(launches))

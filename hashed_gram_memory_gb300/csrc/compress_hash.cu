@@ -70,9 +70,12 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
       const int ni = (r >= p.H) + (r >= 2 * p.H);  // n - 2
       const int j = r - ni * p.H;
       uint64_t h = p.seed[ni][j];
-      for (int k = 2 - ni; k < 4; ++k) {  // the last n = ni + 2 ids, oldest first
-        h = (h ^ (uint64_t)(uint32_t)w[k]) * kFold;
-        h ^= h >> 29;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // the last n = ni + 2 ids, oldest first
+        if (k >= 2 - ni) {
+          h = (h ^ (uint64_t)(uint32_t)w[k]) * kFold;
+          h ^= h >> 29;
+        }
       }
       p.row_ids[t * R + r] = (int32_t)(h % p.rows[ni]);
     } else {

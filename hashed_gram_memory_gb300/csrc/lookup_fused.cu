@@ -13,11 +13,8 @@
 // token spans several warps).  Rows are read with L1::no_allocate (no reuse
 // inside an SM); streams with .cs (evict-first) so they do not push hot table
 // rows out of L2.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
-
 #include "engram_internal.cuh"
+#include "lookup_common.cuh"
 
 namespace engram {
 namespace {
@@ -28,41 +25,6 @@ __device__ __forceinline__ uint4 ld_row16(const uint8_t *ptr) {
       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
       : "l"(ptr));
   return v;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// acc[0..16) += scale * e4m3(v[0..16)), exact e4m3 -> f16 -> f32 widening.
-__device__ __forceinline__ void acc_fp8(float (&acc)[16], const uint4 &v, float scale) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const __half2_raw lo =
-        __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xFFFFu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-    acc[4 * q + 0] = fmaf(a.x, scale, acc[4 * q + 0]);
-    acc[4 * q + 1] = fmaf(a.y, scale, acc[4 * q + 1]);
-    acc[4 * q + 2] = fmaf(b.x, scale, acc[4 * q + 2]);
-    acc[4 * q + 3] = fmaf(b.y, scale, acc[4 * q + 3]);
-  }
-}
-
-// acc[0..8) += bf16(v[0..8)).
-__device__ __forceinline__ void acc_bf16(float *acc, const uint4 &v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    acc[2 * q + 0] += bf16_lo(w[q]);
-    acc[2 * q + 1] += bf16_hi(w[q]);
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 template <int DT, bool AUX>
@@ -155,16 +117,7 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
   if (work) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] *= p.inv_R;
-    const uint32_t a32[8] = {xs[0][0].x, xs[0][0].y, xs[0][0].z, xs[0][0].w,
-                             xs[0][1].x, xs[0][1].y, xs[0][1].z, xs[0][1].w};
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float a0 = bf16_lo(a32[q]), a1 = bf16_hi(a32[q]);
-      const float m0 = acc[2 * q], m1 = acc[2 * q + 1];
-      saa = fmaf(a0, a0, fmaf(a1, a1, saa));
-      smm = fmaf(m0, m0, fmaf(m1, m1, smm));
-      sam = fmaf(a0, m0, fmaf(a1, m1, sam));
-    }
+    gate_partials(xs[0][0], xs[0][1], acc, saa, smm, sam);
   }
 
   // Sum over the token's tpt threads.
@@ -193,28 +146,14 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
 
   if (!work) return;
 
-  // g = sigmoid( sum(a m) / (rms(a) rms(m) sqrt(D)) ), rms(x) = sqrt(mean(x^2) + eps).
-  const float Df = (float)p.D;
-  const float rms_a = sqrtf(saa / Df + p.eps);
-  const float rms_m = sqrtf(smm / Df + p.eps);
-  const float logit = sam / (rms_a * rms_m * p.sqrt_D);
-  const float g = 1.f / (1.f + expf(-logit));
+  const float g = gate_value(saa, smm, sam, (float)p.D, p.eps, p.sqrt_D);
 
   uint16_t *yrow = p.y + t * 4 * p.D + col0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     const float c = g * __ldg(p.alpha + s);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 in = xs[s][h];
-      const float *mm = acc + 8 * h;
-      uint4 out;
-      out.x = pack_bf16(fmaf(c, mm[0], bf16_lo(in.x)), fmaf(c, mm[1], bf16_hi(in.x)));
-      out.y = pack_bf16(fmaf(c, mm[2], bf16_lo(in.y)), fmaf(c, mm[3], bf16_hi(in.y)));
-      out.z = pack_bf16(fmaf(c, mm[4], bf16_lo(in.z)), fmaf(c, mm[5], bf16_hi(in.z)));
-      out.w = pack_bf16(fmaf(c, mm[6], bf16_lo(in.w)), fmaf(c, mm[7], bf16_hi(in.w)));
-      __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * p.D + 8 * h), out);
-    }
+    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * p.D), gated_add8(xs[s][0], acc, c));
+    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * p.D + 8), gated_add8(xs[s][1], acc + 8, c));
   }
   if (AUX) {
     if (p.gate_out && lane_t == 0) p.gate_out[t] = g;
@@ -258,9 +197,6 @@ cudaError_t launch_lookup(const LookupParams &p_in, int dtype, cudaStream_t stre
   p.tpt = tpt;
   p.tpb = tpb;
   const int threads = p.tpb * tpt;
-  p.inv_R = 1.f / (float)R;
-  p.inv_D = 1.f / (float)p.D;
-  p.sqrt_D = sqrtf((float)p.D);
   const size_t smem = (size_t)p.tpb * R * sizeof(int32_t) + 8 * 3 * sizeof(float);
   const bool aux = p.gate_out != nullptr || p.mem_out != nullptr;
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN)

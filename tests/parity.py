@@ -4,9 +4,10 @@ through the CPU oracle on the same seeded inputs, and compare.
 Tolerances (the streams are bf16 outputs of fp32 arithmetic):
 * compressed ids, row ids, history: bit-exact;
 * streams: |y - y_ref| <= 2e-2 + 1e-2 |y_ref| elementwise (the stated max-abs
-  2e-2 / rel 1e-2 bar, read as an allclose), and in addition no element more
-  than one bf16 ulp from the oracle's once-rounded value, and at most 0.1% of
-  elements not bit-identical (the fp32 path rounds twice: fp32, then bf16);
+  2e-2 / rel 1e-2 bar, read as an allclose), and in addition within one bf16
+  ulp of the oracle's once-rounded value plus the fp32 rounding of the operands
+  (2^-23 |x| + 2^-16 |y - x|), and at most 0.1% of elements not bit-identical
+  (the fp32 path rounds twice: fp32, then bf16);
 * m (fp32, sum of 3H products): within 1e-5 relative + 1e-6 of max |m|;
 * g (fp32 sigmoid of a 4096-term fp32 reduction): within 1e-5 absolute.
 """
@@ -93,7 +94,7 @@ def gpu_path(cfg: W.EngramConfig, dev: dict, aux: bool = True, in_place: bool = 
     eg.engram_lookup_fused(rows, cfg.H, dev["tables"], src, dev["alpha"], cfg.eps, streams_out=out,
                            gate_out=gate, mem_out=mem, status=status)
     code, flags = eg.engram_read_status(status)
-    res = dict(eids=eids.cpu().numpy(), rows=rows.cpu().numpy(),
+    res = dict(eids=eids.cpu().numpy(), rows=rows.cpu().numpy(), x=x.cpu().numpy().view(np.uint16),
                history=None if hist_out is None else hist_out.cpu().numpy(),
                streams=out.cpu().numpy().view(np.uint16), flags=flags, code=code)
     if aux:
@@ -108,16 +109,23 @@ def bf16_ulp(y: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, e - 8)
 
 
-def compare_streams(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str = "streams"):
+def compare_streams(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, x_bits: np.ndarray,
+                    what: str = "streams"):
+    """The stated allclose bar, then a tight one: one bf16 ulp of the oracle's
+    value plus the fp32 path's own error, which scales with its operands (x and
+    the update g*alpha*m ~ y - x), not with y: near cancellation the ulp of y is
+    far below fp32's rounding of x."""
     yg = oracle.bf16_bits_to_float(y_gpu_bits).astype(np.float64)
     yr = oracle.bf16_bits_to_float(y_ref_bits).astype(np.float64)
+    x = oracle.bf16_bits_to_float(x_bits).astype(np.float64)
     assert np.isfinite(yg).all(), f"{what}: non-finite output"
     err = np.abs(yg - yr)
     bound = STREAM_ATOL + STREAM_RTOL * np.abs(yr)
     worst = float(np.max(err / bound)) if err.size else 0.0
     assert np.all(err <= bound), f"{what}: allclose bar exceeded, worst err/bound {worst:.3g}"
-    ulp = bf16_ulp(yr)
-    assert np.all(err <= ulp * 1.0000001), f"{what}: max err {np.max(err / ulp):.3g} ulp"
+    tight = bf16_ulp(yr) + 2.0 ** -23 * np.abs(x) + 2.0 ** -16 * np.abs(yr - x)
+    worst = float(np.max(err / tight)) if err.size else 0.0
+    assert np.all(err <= tight), f"{what}: tight bound exceeded by {worst:.3g}x"
     mism = float(np.mean(y_gpu_bits != y_ref_bits)) if err.size else 0.0
     assert mism <= MAX_MISMATCH_FRAC, f"{what}: {mism:.2e} of elements not bit-identical"
     return dict(max_abs=float(err.max()) if err.size else 0.0, mismatch_frac=mism)
@@ -138,7 +146,7 @@ def compare_all(res: dict, ref: dict, aux: bool = True):
     assert np.array_equal(res["rows"], ref["rows"])
     if ref["history"] is not None and res["history"] is not None:
         assert np.array_equal(res["history"], ref["history"])
-    stats = compare_streams(res["streams"], ref["streams"])
+    stats = compare_streams(res["streams"], ref["streams"], res["x"])
     if aux:
         compare_mem(res["mem"], ref["mem"])
         compare_gate(res["gate"], ref["gate"])

@@ -96,7 +96,7 @@ def test_lookup_flags_bad_rows_and_leaves_token_unwritten(eg):
     got = out.cpu().numpy().view(np.uint16)
     assert (got[3] == 0x1234).all() and (got[20] == 0x1234).all()
     keep = [t for t in range(cfg.T) if t not in (3, 20)]
-    P.compare_streams(got[keep], ref[keep])
+    P.compare_streams(got[keep], ref[keep], inp.streams.reshape(cfg.T, 4, cfg.D)[keep])
 
 
 @pytest.mark.parametrize("split", [0, 1, 2, 3, 9])
@@ -147,3 +147,28 @@ def test_zero_alpha_and_zero_rows_leave_streams_bit_identical(eg, dtype):
     res = P.gpu_path(base, dev, aux=True)
     assert np.array_equal(res["streams"], inp.streams)
     assert np.all(res["mem"] == 0) and np.allclose(res["gate"], 0.5)
+
+
+def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg):
+    """A withheld row copy (the mbarrier expects bytes that never come) makes the
+    consumers' bounded wait run out: the launch ends by itself with
+    ENGRAM_FLAG_TIMEOUT, and the next launch on the same context is exact."""
+    import torch
+    cfg = W.CONFIGS[3].scaled(B=1, S=700, rows=(1009, 1013, 1019))
+    inp = P.host_inputs(cfg)
+    ref = P.oracle_path(inp)
+    dev = P.to_device(inp)
+    prev_k = eg.engram_set_lookup_kernel(eg.LOOKUP_BULK)
+    prev_l = eg.engram_set_wait_limit_ns(5_000_000)
+    try:
+        eg.engram_debug_withhold_copies(1)
+        res = P.gpu_path(cfg, dev, aux=False)
+        assert res["code"] == eg.ERR_TIMEOUT and res["flags"] & eg.FLAG_TIMEOUT
+        torch.cuda.synchronize()
+        again = P.gpu_path(cfg, dev, aux=True)
+        assert again["flags"] == 0
+        P.compare_all(again, ref)
+    finally:
+        eg.engram_debug_withhold_copies(0)
+        eg.engram_set_wait_limit_ns(prev_l)
+        eg.engram_set_lookup_kernel(prev_k)

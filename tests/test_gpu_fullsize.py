@@ -97,6 +97,6 @@ def test_full_size_sampled(eg, ci):
                               scs, x, d["alpha"].cpu().numpy(), cfg.eps)
     assert f3 == 0
     y = out.view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
-    P.compare_streams(y, y_ref, what=f"{cfg.name} sampled streams")
+    P.compare_streams(y, y_ref, x, what=f"{cfg.name} sampled streams")
     del d, out, rows, eids
     torch.cuda.empty_cache()

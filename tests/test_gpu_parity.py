@@ -38,8 +38,16 @@ def eg():
     return eg
 
 
+@pytest.fixture(params=["gather", "bulk"])
+def kernel(eg, request):
+    which = {"gather": eg.LOOKUP_GATHER, "bulk": eg.LOOKUP_BULK}[request.param]
+    prev = eg.engram_set_lookup_kernel(which)
+    yield request.param
+    eg.engram_set_lookup_kernel(prev)
+
+
 @pytest.mark.parametrize("name", list(SMALL))
-def test_parity_vs_oracle(eg, name):
+def test_parity_vs_oracle(eg, kernel, name):
     cfg = SMALL[name]
     inp = P.host_inputs(cfg)
     ref = P.oracle_path(inp)
@@ -50,8 +58,24 @@ def test_parity_vs_oracle(eg, name):
     assert np.array_equal(res2["streams"], res["streams"])
 
 
-@pytest.mark.parametrize("name", ["tiny_fp8_d256", "bf16_tables", "d1040_h5"])
-def test_in_place_streams(eg, name):
+@pytest.mark.parametrize("name", [n for n, c in SMALL.items() if c.D % 512 == 0])
+def test_bulk_and_gather_kernels_agree_bit_for_bit(eg, name):
+    cfg = SMALL[name]
+    dev = P.to_device(P.host_inputs(cfg))
+    out = {}
+    for which in (eg.LOOKUP_GATHER, eg.LOOKUP_BULK):
+        prev = eg.engram_set_lookup_kernel(which)
+        try:
+            out[which] = P.gpu_path(cfg, dev, aux=True)
+        finally:
+            eg.engram_set_lookup_kernel(prev)
+    a, b = out[eg.LOOKUP_GATHER], out[eg.LOOKUP_BULK]
+    for key in ("streams", "gate", "mem"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("name", ["tiny_fp8_d256", "bf16_tables", "d1040_h5", "full_prefill_fp8"])
+def test_in_place_streams(eg, kernel, name):
     cfg = SMALL[name]
     inp = P.host_inputs(cfg)
     dev = P.to_device(inp)
