@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[c.name for c in W.CONFIGS])
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
@@ -323,46 +323,47 @@ def run_native(args):
 
 
 def run_e2e(eg, cfg, step, stream, steps, world, device):
-    """Same metric through the C ABI with host buffers: every step copies the token
-    ids and the four input streams from pinned host memory, runs the three calls,
-    and copies the updated streams back, all inside the timed region."""
+    """Same metric through the C ABI with HOST buffers: every step is one
+    engram_forward_host call that copies the token ids and the four input streams
+    from pinned host memory, runs compress + hash + the fused lookup, and copies
+    the updated streams back (chunked, copies overlapped with the lookup), all
+    inside the timed region."""
     import torch
-    import torch.distributed as dist
     from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
     d = step.d
     ids_h = d["ids"].cpu().pin_memory()
     x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
     x_h.copy_(d["streams"])
-    y_h = torch.empty_like(x_h, pin_memory=True)
-    ids_d = torch.empty_like(d["ids"])
-    x_d = torch.empty_like(d["streams"])
-    y_d = torch.empty_like(d["streams"])
+    y_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    ws = torch.empty(eg.engram_forward_host_workspace_bytes(cfg.B, cfg.S, cfg.H, cfg.D, 0),
+                     dtype=torch.uint8, device=device)
 
     def one():
-        ids_d.copy_(ids_h, non_blocking=True)
-        x_d.copy_(x_h, non_blocking=True)
-        step(ids=ids_d, x=x_d, out=y_d)
-        y_h.copy_(y_d, non_blocking=True)
+        eg.engram_forward_host(ids_h, d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], x_h, y_h,
+                               d["alpha"], ws, cfg.eps, history=d["history"],
+                               history_out=step.hist_out, status=step.status, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            one()
-    torch.cuda.synchronize()
+    for _ in range(2):
+        one()
+    stream.synchronize()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(steps):
-            one()
+    for _ in range(steps):
+        one()
     stream.synchronize()
     dt = time.perf_counter() - t0
     dt = max_over_ranks(dt, device)
+    ok = torch.equal(y_h.to(device), step.out)   # same result as the device-resident step
     h2d = ids_h.numel() * 4 + x_h.numel() * 2
     d2h = y_h.numel() * 2
-    return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps,
-            "how": "pinned host ids + streams -> device, compress/hash/lookup, streams -> host; "
-                   "one CUDA stream, timed on the host around the steps"}
+    return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "matches_device_step": bool(ok),
+            "how": "engram_forward_host: pinned host ids + streams in, compress/hash/lookup, "
+                   "streams out; 2048-token chunks, copies overlapped with the lookup on two "
+                   "copy streams; host timer around the steps + a final stream sync"}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -464,7 +465,7 @@ def run_reference(args, budget_s: float = 60.0):
     K = max(1, args.steps)
     probe = reference_sample(cfg, min(256, cfg.T))
     rate = probe["n"] / time_oracle(cfg, probe)
-    n = int(max(16, min(cfg.T, 4096, budget_s * rate / K)))
+    n = int(max(16, min(cfg.T, 32768, budget_s * rate / K)))
     s = reference_sample(cfg, n)
     for _ in range(max(1, min(args.warmup, 3))):
         time_oracle(cfg, s)

@@ -59,6 +59,18 @@ def _load():
     L.engram_set_wait_limit_ns.restype = C.c_int64
     L.engram_debug_withhold_copies.argtypes = [C.c_int32]
     L.engram_debug_withhold_copies.restype = None
+    sz = C.c_size_t
+    L.engram_forward_workspace_bytes.argtypes = [i32, i32, i32]
+    L.engram_forward_workspace_bytes.restype = sz
+    L.engram_forward.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, C.POINTER(engram_tables),
+                                 vp, vp, vp, C.c_float, vp, sz, vp, vp]
+    L.engram_forward.restype = i32
+    L.engram_forward_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.engram_forward_host_workspace_bytes.restype = sz
+    L.engram_forward_host.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
+                                      C.POINTER(engram_tables), vp, vp, vp, C.c_float, i32, vp, sz,
+                                      vp, vp]
+    L.engram_forward_host.restype = i32
     return L
 
 
@@ -215,3 +227,51 @@ def engram_set_wait_limit_ns(ns: int) -> int:
 
 def engram_debug_withhold_copies(launches: int) -> None:
     lib.engram_debug_withhold_copies(int(launches))
+
+
+def engram_forward_workspace_bytes(batch: int, seq: int, n_heads: int) -> int:
+    return int(lib.engram_forward_workspace_bytes(batch, seq, n_heads))
+
+
+def engram_forward(token_ids, tid2eid, n_eids: int, n_heads: int, tables: Tables, streams_in,
+                   alpha, eps: float = 1e-6, history=None, history_out=None, streams_out=None,
+                   workspace=None, status=None, stream=None):
+    """compress -> hash -> fused lookup in one call on device tensors; token_ids [B, S]."""
+    import torch
+    _need(token_ids, (torch.int32,), "token_ids")
+    B, S = token_ids.shape
+    if streams_out is None:
+        streams_out = torch.empty_like(streams_in)
+    need = engram_forward_workspace_bytes(B, S, n_heads)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=token_ids.device)
+    s = tables.struct()
+    _check(lib.engram_forward(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
+                              _ptr(history), _ptr(history_out), n_heads, C.byref(s),
+                              _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
+                              _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)),
+           "engram_forward")
+    return streams_out
+
+
+def engram_forward_host_workspace_bytes(batch: int, seq: int, n_heads: int, D: int,
+                                        chunk_tokens: int = 0) -> int:
+    return int(lib.engram_forward_host_workspace_bytes(batch, seq, n_heads, D, chunk_tokens))
+
+
+def engram_forward_host(token_ids_host, tid2eid, n_eids: int, n_heads: int, tables: Tables,
+                        streams_in_host, streams_out_host, alpha, workspace, eps: float = 1e-6,
+                        history=None, history_out=None, chunk_tokens: int = 0, status=None,
+                        stream=None):
+    """The whole path with host (CPU, ideally pinned) token ids [B, S] and streams
+    [B*S, 4, D]; workspace is a device uint8 tensor of
+    engram_forward_host_workspace_bytes(...) bytes.  Asynchronous on `stream`."""
+    B, S = token_ids_host.shape
+    s = tables.struct()
+    _check(lib.engram_forward_host(_ptr(token_ids_host), B, S, _ptr(tid2eid), tid2eid.numel(),
+                                   n_eids, _ptr(history), _ptr(history_out), n_heads, C.byref(s),
+                                   _ptr(streams_in_host), _ptr(streams_out_host), _ptr(alpha),
+                                   float(eps), chunk_tokens, _ptr(workspace), workspace.numel(),
+                                   _ptr(status), _stream(stream)),
+           "engram_forward_host")
+    return streams_out_host

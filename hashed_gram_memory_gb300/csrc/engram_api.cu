@@ -41,22 +41,10 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 // Per-device memo of the architecture check: 0 unknown, 1 sm_103, 2 other.
 std::atomic<int> g_arch_ok[64];
-std::atomic<int> g_num_sms[64];
 
 std::atomic<int> g_lookup_kernel{ENGRAM_LOOKUP_AUTO};
 std::atomic<int64_t> g_wait_limit_ns{250000000};
 std::atomic<int> g_withhold{0};
-
-int num_sms() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  int n = g_num_sms[dev & 63].load(std::memory_order_relaxed);
-  if (n == 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
-    g_num_sms[dev & 63].store(n, std::memory_order_relaxed);
-  }
-  return n;
-}
 
 engram_status check_device() {
   int dev = 0;
@@ -85,6 +73,14 @@ engram_status launched(const char *what, cudaError_t e) {
 }
 
 }  // namespace
+
+engram_status engram::set_error(engram_status code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
 
 extern "C" {
 
@@ -253,17 +249,15 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   p.sqrt_D = sqrtf((float)D);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   const int which = g_lookup_kernel.load(std::memory_order_relaxed);
-  const int sms = num_sms();
-  const bool bulk = engram::bulk_supported(D) &&
-                    (which == ENGRAM_LOOKUP_BULK ||
-                     (which == ENGRAM_LOOKUP_AUTO && n_tokens >= 2 * (int64_t)sms));
+  const bool bulk = engram::bulk_supported(D, tb.dtype, n_heads) &&
+                    (which == ENGRAM_LOOKUP_BULK || which == ENGRAM_LOOKUP_AUTO);
   if (bulk) {
     int w = g_withhold.load(std::memory_order_relaxed);
     while (w > 0 && !g_withhold.compare_exchange_weak(w, w - 1)) {
     }
     p.withhold = w > 0 ? 1 : 0;
     return launched("engram_lookup_fused launch (bulk)",
-                    engram::launch_lookup_bulk(p, tb.dtype, sms, (cudaStream_t)stream));
+                    engram::launch_lookup_bulk(p, tb.dtype, (cudaStream_t)stream));
   }
   return launched("engram_lookup_fused launch (gather)",
                   engram::launch_lookup(p, tb.dtype, (cudaStream_t)stream));

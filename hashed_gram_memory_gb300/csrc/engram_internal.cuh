@@ -52,9 +52,6 @@ struct LookupParams {
   int32_t H, D;
   int32_t tpt;  // gather kernel: threads per token (16 columns each)
   int32_t tpb;  // gather kernel: tokens per block
-  int32_t nw;       // bulk kernel: consumer warps (D / 512)
-  int32_t nslot;    // bulk kernel: row slots in the shared-memory ring
-  int32_t nstage;   // bulk kernel: stream stages
   int32_t withhold; // bulk kernel test hook: withhold one row copy per block
   int64_t wait_limit_ns;
   float eps, inv_R, inv_D, sqrt_D;
@@ -63,8 +60,11 @@ struct LookupParams {
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t stream);
 cudaError_t launch_hash(const HashParams &p, cudaStream_t stream);
 cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream);
-cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, int num_sms, cudaStream_t stream);
-bool bulk_supported(int D);
+cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
+bool bulk_supported(int D, int dtype, int H);
+
+// Records the message engram_last_error() returns on this thread; returns code.
+engram_status set_error(engram_status code, const char *fmt, ...);
 
 // splitmix64 first output for state x (S. Vigna, public domain), used for the
 // per-(order, head) hash seeds on the host.

@@ -42,6 +42,7 @@
 #ifndef ENGRAM_H
 #define ENGRAM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -160,6 +161,48 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
                                              float *mem_out, int32_t *status, void *stream);
 
 /*
+ * engram_forward -- the whole path in one call on device buffers:
+ * engram_compress, engram_hash and engram_lookup_fused back to back on
+ * `stream`, with the compressed ids and row ids kept in `workspace` (device
+ * memory of at least engram_forward_workspace_bytes(batch, seq, n_heads) bytes,
+ * 16-byte aligned, owned by the caller, not read after the call's kernels end).
+ *   token_ids int32 [batch, seq] (device); history / history_out as in
+ *   engram_hash; streams as in engram_lookup_fused ([batch*seq, 4, D]).
+ */
+ENGRAM_API size_t engram_forward_workspace_bytes(int32_t batch, int32_t seq, int32_t n_heads);
+ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch, int32_t seq,
+                                        const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
+                                        const int32_t *history, int32_t *history_out,
+                                        int32_t n_heads, const engram_tables *tables_host,
+                                        const uint16_t *streams_in, uint16_t *streams_out,
+                                        const float *alpha, float eps, void *workspace,
+                                        size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
+ * engram_forward_host -- the whole path with the token ids and the streams in
+ * HOST memory (pinned for overlap; pageable works but serialises the copies).
+ * The call copies the ids in, runs compress + hash, then pipelines the streams
+ * in chunks of `chunk_tokens` tokens (0 = 2048): host->device copies on one
+ * internal copy stream, the fused lookup on `stream`, device->host copies on a
+ * second copy stream, with three chunk buffers per direction in `workspace`
+ * (device memory of at least engram_forward_host_workspace_bytes(...) bytes).
+ * Returns once everything is enqueued; `stream` is ordered after the last
+ * device->host copy, so synchronising `stream` means streams_out_host is final.
+ * The two copy streams and their events are created on first use per device
+ * and kept for the life of the process.  tid2eid, history, history_out, the
+ * tables, alpha and status are device memory as in the calls above.
+ */
+ENGRAM_API size_t engram_forward_host_workspace_bytes(int32_t batch, int32_t seq,
+                                                      int32_t n_heads, int32_t D,
+                                                      int32_t chunk_tokens);
+ENGRAM_API engram_status engram_forward_host(
+    const int32_t *token_ids_host, int32_t batch, int32_t seq, const int32_t *tid2eid,
+    int32_t vocab, int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
+    const engram_tables *tables_host, const uint16_t *streams_in_host,
+    uint16_t *streams_out_host, const float *alpha, float eps, int32_t chunk_tokens,
+    void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
  * engram_read_status -- waits for `stream`, copies the device status word into
  * *flags_host and returns ENGRAM_OK (no flag), ENGRAM_ERR_TIMEOUT
  * (ENGRAM_FLAG_TIMEOUT set) or ENGRAM_ERR_OUT_OF_RANGE (a range flag set).  The
@@ -170,12 +213,13 @@ ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flag
 
 /*
  * Kernel choice of engram_lookup_fused for this process:
- *   ENGRAM_LOOKUP_AUTO    the library picks (default);
- *   ENGRAM_LOOKUP_GATHER  register-direct gathers, one token per thread group
- *                         (any D);
- *   ENGRAM_LOOKUP_BULK    persistent kernel: one producer warp streams rows and
- *                         streams into a shared-memory ring with 1-D bulk copies
- *                         (TMA) under mbarriers; D % 512 == 0 only, otherwise the
+ *   ENGRAM_LOOKUP_AUTO    the library picks (default: BULK where it applies);
+ *   ENGRAM_LOOKUP_GATHER  register-direct gathers, one token per thread group,
+ *                         rows loaded in batches of 8 (any D);
+ *   ENGRAM_LOOKUP_BULK    one token per block: one thread stages all 3H rows in
+ *                         shared memory with 1-D bulk copies (TMA) on a single
+ *                         mbarrier while the others load the streams; needs
+ *                         D % 512 == 0 and 3H*D*elt <= ~227 KB, otherwise the
  *                         call falls back to GATHER.
  * Both give identical results.  Returns the previous setting, or -1 for an
  * unknown value (nothing changed).  Not synchronised with calls in flight on
@@ -197,8 +241,9 @@ ENGRAM_API int64_t engram_set_wait_limit_ns(int64_t ns);
 /*
  * Test hook for the timeout path: the next `launches` launches of the BULK
  * lookup kernel withhold one row copy in every block (the mbarrier still
- * expects its bytes), so the consumers' bounded wait runs out and the launch
- * reports ENGRAM_FLAG_TIMEOUT.  For tests only; 0 turns it off.
+ * expects its bytes), so the block's bounded wait runs out, the block skips its
+ * token, and the launch reports ENGRAM_FLAG_TIMEOUT.  For tests only; 0 turns
+ * it off.
  */
 ENGRAM_API void engram_debug_withhold_copies(int32_t launches);
 

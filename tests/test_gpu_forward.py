@@ -1,0 +1,86 @@
+"""The one-call entry points: engram_forward (device buffers) must equal the three
+separate calls bit for bit; engram_forward_host (host ids and streams, chunked
+copy/compute pipeline) must equal engram_forward bit for bit, for ragged chunk
+sizes, pinned and pageable host memory, and back-to-back calls that reuse the
+same workspace with different inputs."""
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def eg():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import hashed_gram_memory_gb300 as eg
+    return eg
+
+
+CASES = {
+    "prefill_h8": W.CONFIGS[3].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "decode_history": W.CONFIGS[2].scaled(B=300, rows=(7001, 7013, 7019)),
+    "bf16": W.CONFIGS[4].scaled(B=3, S=133, rows=(3001, 3011, 3019)),
+    "tiny_d256": W.CONFIGS[0],
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_equals_separate_calls_and_oracle(eg, name):
+    import torch
+    cfg = CASES[name]
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    sep = P.gpu_path(cfg, dev, aux=False)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist_out = torch.empty_like(dev["history"]) if dev["history"] is not None else None
+    y = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                          dev["streams"], dev["alpha"], cfg.eps, history=dev["history"],
+                          history_out=hist_out, status=st)
+    code, flags = eg.engram_read_status(st)
+    assert flags == 0
+    assert np.array_equal(y.cpu().numpy().view(np.uint16), sep["streams"])
+    if hist_out is not None:
+        assert np.array_equal(hist_out.cpu().numpy(), sep["history"])
+    ref = P.oracle_path(inp)
+    P.compare_streams(sep["streams"], ref["streams"], inp.streams)
+
+
+@pytest.mark.parametrize("name,chunk,pinned", [("prefill_h8", 77, True), ("prefill_h8", 0, False),
+                                               ("decode_history", 64, True), ("bf16", 128, True),
+                                               ("tiny_d256", 1, True)])
+def test_forward_host_equals_forward(eg, name, chunk, pinned):
+    import torch
+    cfg = CASES[name]
+    outs_dev, outs_host = [], []
+    ws = torch.empty(eg.engram_forward_host_workspace_bytes(cfg.B, cfg.S, cfg.H, cfg.D, chunk),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    hosts = []
+    # two back-to-back calls with different inputs (replica 0 and 1) on one workspace
+    for rank in (0, 1):
+        inp = P.host_inputs(cfg, rank=rank)
+        dev = P.to_device(inp)
+        outs_dev.append(eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H,
+                                          dev["tables"], dev["streams"], dev["alpha"], cfg.eps,
+                                          history=dev["history"]).cpu().numpy().view(np.uint16))
+        ids_h = torch.from_numpy(inp.ids)
+        x_h = torch.from_numpy(inp.streams.view(np.int16)).reshape(cfg.T, 4, cfg.D)
+        if pinned:
+            ids_h, x_h = ids_h.pin_memory(), x_h.pin_memory()
+        y_h = torch.full_like(x_h, 0x7777)
+        if pinned:
+            y_h = y_h.pin_memory()
+        hosts.append((ids_h, x_h, y_h, dev))
+    with torch.cuda.stream(stream):
+        for ids_h, x_h, y_h, dev in hosts:
+            eg.engram_forward_host(ids_h, dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"], x_h,
+                                   y_h, dev["alpha"], ws, cfg.eps, history=dev["history"],
+                                   chunk_tokens=chunk)
+    stream.synchronize()
+    for (ids_h, x_h, y_h, dev), ref in zip(hosts, outs_dev):
+        assert np.array_equal(y_h.numpy().view(np.uint16).reshape(ref.shape), ref)
