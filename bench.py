@@ -36,7 +36,6 @@ DEFAULT_WORKLOAD = "full_prefill_fp8"
 METRIC = "Engram fused lookup tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lookup_fused_traffic.json")
-LOOKUP_SRC = os.path.join(ROOT, "hashed_gram_memory_gb300", "csrc", "lookup_fused.cu")
 
 
 def parse():
@@ -91,16 +90,22 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(cfg):
+def recorded_traffic(cfg, kernel: str):
     """Per-launch DRAM bytes of the lookup kernel from the committed ncu summary,
-    or None when the kernel source changed since it was taken."""
-    if not os.path.exists(TRAFFIC_FILE):
+    scaled by tokens, or None when the kernel timed is not the one captured or its
+    sources changed since the capture."""
+    if kernel not in ("auto", "bulk") or not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
-    sha = hashlib.sha256(open(LOOKUP_SRC, "rb").read()).hexdigest()
     rec = d.get(cfg.name)
-    if not rec or rec.get("lookup_fused_cu_sha256") != sha:
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec["kernel_sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec.get("kernel_sources_sha256"):
         return None
     return float(rec["dram_bytes_per_token"]) * cfg.T
 
@@ -278,7 +283,7 @@ def run_native(args):
         bytes_tok = cfg.algorithmic_bytes_per_token()
         lk = statistics.mean(lookup_ms)
         achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
-        traffic = recorded_traffic(cfg)
+        traffic = recorded_traffic(cfg, args.lookup_kernel)
         value = whole_job_throughput(world * cfg.T * K, ms_total * 1e-3)
         line = {
             "metric": METRIC,
@@ -373,15 +378,17 @@ def oracle_sample(cfg, d, n_tokens):
     windows), with exactly the table rows they need copied back from the device."""
     import torch
     import oracle
-    n = min(n_tokens, cfg.S) if not cfg.decode else min(n_tokens, cfg.B)
     if cfg.decode:
+        n = min(n_tokens, cfg.B)
         ids = d["ids"][:n].cpu().numpy()
         hist = d["history"][:n].cpu().numpy()
         x = d["streams"][:n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
     else:
-        ids = d["ids"][:1, :n].cpu().numpy()
+        nseq = max(1, min(cfg.B, -(-n_tokens // cfg.S)))   # whole sequences: windows self-contained
+        n = nseq * cfg.S
+        ids = d["ids"][:nseq].cpu().numpy()
         hist = None
-        x = d["streams"][0, :n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
+        x = d["streams"][:nseq].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
     tid2eid = d["tid2eid"].cpu().numpy()
     e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
     r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist)
@@ -420,7 +427,7 @@ def cpu_baseline(cfg, d, n_tokens):
     dt = time_oracle(cfg, s)
     return {"value": s["n"] / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"first {s['n']} tokens of the {cfg.name} batch (same seeded inputs, the "
+            "sample": f"first {s['n']} tokens (whole sequences) of the {cfg.name} batch (same seeded inputs, the "
                       f"rows they need copied from the device): compress + hash + fused lookup in "
                       f"the fp64 C oracle, {dt:.2f} s wall"}
 
