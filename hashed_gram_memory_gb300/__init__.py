@@ -71,6 +71,9 @@ def _load():
                                       C.POINTER(engram_tables), vp, vp, vp, C.c_float, i32, vp, sz,
                                       vp, vp]
     L.engram_forward_host.restype = i32
+    L.engram_forward_static.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
+                                        C.POINTER(engram_tables), vp, vp, vp, C.c_float, vp, vp]
+    L.engram_forward_static.restype = i32
     return L
 
 
@@ -275,3 +278,25 @@ def engram_forward_host(token_ids_host, tid2eid, n_eids: int, n_heads: int, tabl
                                    _ptr(status), _stream(stream)),
            "engram_forward_host")
     return streams_out_host
+
+
+STATIC_WORKSPACE_BYTES = 16 << 20
+
+
+def engram_forward_static(token_ids, tid2eid, n_eids: int, n_heads: int, tables: Tables,
+                          streams_in, alpha, eps: float = 1e-6, history=None, history_out=None,
+                          streams_out=None, status=None, stream=None):
+    """engram_forward without a workspace: the library's fixed device array holds
+    the ids (for callers that must not allocate device memory; see engram.h)."""
+    import torch
+    _need(token_ids, (torch.int32,), "token_ids")
+    B, S = token_ids.shape
+    if streams_out is None:
+        streams_out = torch.empty_like(streams_in)
+    s = tables.struct()
+    _check(lib.engram_forward_static(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
+                                     _ptr(history), _ptr(history_out), n_heads, C.byref(s),
+                                     _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
+                                     _ptr(status), _stream(stream)),
+           "engram_forward_static")
+    return streams_out

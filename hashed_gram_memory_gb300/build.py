@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libengram.so")
 
-SOURCES = ["engram_api.cu", "compress_hash.cu", "lookup_fused.cu", "lookup_bulk.cu", "forward.cu"]
+SOURCES = ["engram_api.cu", "compress_hash.cu", "lookup_fused.cu", "lookup_bulk.cu", "forward.cu",
+           "forward_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

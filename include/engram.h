@@ -203,6 +203,36 @@ ENGRAM_API engram_status engram_forward_host(
     void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
+ * engram_forward_static -- engram_forward without a workspace argument, for
+ * callers that cannot call cudaMalloc: a plugin or kernel library loaded into a
+ * host program that owns all device memory and hands it only input and output
+ * buffers, a runtime whose memory pool forbids allocations outside it, or code
+ * that must not allocate after start-up (an allocation can synchronise the
+ * device or fail at an awkward time).  The pages have no counterpart; it is a
+ * calling convenience.
+ *
+ * Instead of a caller workspace it uses one file-scope device array of
+ * ENGRAM_STATIC_WORKSPACE_BYTES (16 MiB), which every device that loads the
+ * library holds until the process exits.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.  Its first call on a
+ * device looks up the array's device address there (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * Requests needing more than the array, engram_forward_workspace_bytes(batch,
+ * seq, n_heads) > ENGRAM_STATIC_WORKSPACE_BYTES (about 160K tokens at 8 heads),
+ * return ENGRAM_ERR_UNSUPPORTED with a message and launch nothing.  All calls
+ * share the one array, which keeps the last call's contents; each call clears
+ * the part it uses on `stream` first.  Calls that overlap on the GPU (on
+ * different streams or host threads, on one device) race on the array: order
+ * them.  Other arguments and results are exactly those of engram_forward.
+ */
+#define ENGRAM_STATIC_WORKSPACE_BYTES (16u << 20)
+ENGRAM_API engram_status engram_forward_static(
+    const int32_t *token_ids, int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
+    int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
+    const engram_tables *tables_host, const uint16_t *streams_in, uint16_t *streams_out,
+    const float *alpha, float eps, int32_t *status, void *stream);
+
+/*
  * engram_read_status -- waits for `stream`, copies the device status word into
  * *flags_host and returns ENGRAM_OK (no flag), ENGRAM_ERR_TIMEOUT
  * (ENGRAM_FLAG_TIMEOUT set) or ENGRAM_ERR_OUT_OF_RANGE (a range flag set).  The
