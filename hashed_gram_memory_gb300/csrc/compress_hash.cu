@@ -13,6 +13,15 @@ namespace {
 
 constexpr uint64_t kFold = 0x9E3779B97F4A7C15ull;
 
+// x mod d for d >= 1, with m = floor((2^64 - 1) / d).  q = umulhi(x, m) is
+// floor(x/d) or one less (d*m lies within d of 2^64, so x*m/2^64 > x/d - 1), so
+// x - q*d is in [0, 2d) and one conditional subtraction finishes it.
+__device__ __forceinline__ uint64_t mod_by_reciprocal(uint64_t x, uint64_t d, uint64_t m) {
+  const uint64_t q = __umul64hi(x, m);
+  const uint64_t r = x - q * d;
+  return r >= d ? r - d : r;
+}
+
 __device__ __forceinline__ void flag_warp(int32_t *status, uint32_t flags) {
   // One atomic per warp instead of one per thread.
   const uint32_t all = __reduce_or_sync(0xffffffffu, flags);
@@ -77,7 +86,7 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
           h ^= h >> 29;
         }
       }
-      p.row_ids[t * R + r] = (int32_t)(h % p.rows[ni]);
+      p.row_ids[t * R + r] = (int32_t)mod_by_reciprocal(h, p.rows[ni], p.rmul[ni]);
     } else {
       flags = ENGRAM_FLAG_BAD_EID;
     }

@@ -167,6 +167,7 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
   p.H = n_heads;
   for (int n = 0; n < 3; ++n) {
     p.rows[n] = (uint64_t)rows_host[n];
+    p.rmul[n] = UINT64_MAX / p.rows[n];
     for (int j = 0; j < n_heads; ++j) p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
   }
   return launched("engram_hash launch", engram::launch_hash(p, (cudaStream_t)stream));

@@ -34,6 +34,7 @@ struct HashParams {
   int32_t tokens_per_block;  // tokens whose 3H outputs one block owns
   int32_t history_inline;    // 1: seq == 1 and the block writes history_out itself
   uint64_t rows[3];
+  uint64_t rmul[3];  // floor((2^64 - 1) / rows[n]): the reciprocal for h mod rows[n]
   uint64_t seed[3][kMaxHeads];
 };
 

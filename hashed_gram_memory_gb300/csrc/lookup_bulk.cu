@@ -4,18 +4,22 @@
 // One token per CTA of D/16 threads (16 columns each).  Thread 0 issues all 3H
 // row copies of the token at once (one contiguous D*elt-byte run per row, one
 // cp.async.bulk each) completing on a single mbarrier that expects their total
-// byte count; meanwhile every thread loads its four 32-byte stream slices into
-// registers with evict-first loads.  So each CTA has its whole token in flight
-// (3H*D*elt bytes of rows + 8*D bytes of streams: 128 KB for 8 heads of FP8 at
-// D = 4096) from a single issue point, two CTAs share an SM, and the rows cost
-// no registers.  After the wait every thread reads its columns of the rows from
-// shared memory, accumulates the dequantised rows in fp32, the gate sums are
-// reduced across warps, and the four streams are written back with evict-first
-// stores.
+// byte count, while the other threads fetch the row scales into shared memory
+// and, for large tokens, the four 32-byte stream slices into registers with
+// evict-first loads.  After the wait every thread reads its columns of the rows
+// from shared memory, accumulates the dequantised rows in fp32, the gate sums
+// are reduced across warps, and the four streams are written back with
+// evict-first stores.  A whole token is in flight from a single issue point and
+// the rows cost no registers.  Two variants, chosen by the size of a token's
+// rows: two blocks per SM with the streams loaded early (8 heads of FP8 at
+// D = 4096: 96 KB of rows), or four blocks per SM within 64 registers with the
+// streams loaded after the rows (rows within 56 KB).
 //
 // The wait is bounded by the global timer: a copy that never lands makes the
 // block set ENGRAM_FLAG_TIMEOUT, skip the token, and exit only after thread 0
-// has waited (again bounded) for the copies it issued.
+// has waited (again bounded) for the copies it issued.  An id outside its table
+// makes the block set ENGRAM_FLAG_BAD_ROW and skip the token before anything
+// is copied.
 #include "engram_internal.cuh"
 #include "lookup_common.cuh"
 
@@ -75,8 +79,12 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns) {
   }
 }
 
-template <int DT, bool AUX>
-__global__ void __launch_bounds__(256, 2) lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
+// EARLY: the stream slices are loaded into registers before the rows arrive
+// (two blocks per SM); otherwise after them, keeping the block within 64
+// registers per thread so that four blocks share an SM (small tokens).
+template <int DT, bool AUX, bool EARLY>
+__global__ void __launch_bounds__(256, EARLY ? 2 : 4)
+    lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
   constexpr bool kFp8 = DT == ENGRAM_TABLE_FP8_E4M3FN;
   constexpr int kElt = kFp8 ? 1 : 2;
   extern __shared__ __align__(128) uint8_t sm[];
@@ -132,10 +140,12 @@ __global__ void __launch_bounds__(256, 2) lookup_bulk_kernel(const __grid_consta
   }
   uint4 xs[4][2];
   const uint16_t *xrow = p.x + t * 4 * D + col0;
+  if (EARLY) {
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
-    xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+    for (int s = 0; s < 4; ++s) {
+      xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
+      xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+    }
   }
 
   const bool landed = wait_bounded(bar, p.wait_limit_ns);
@@ -166,6 +176,10 @@ __global__ void __launch_bounds__(256, 2) lookup_bulk_kernel(const __grid_consta
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] *= p.inv_R;
 
+  if (!EARLY) {
+    xs[0][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow));
+    xs[0][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + 8));
+  }
   float saa = 0.f, smm = 0.f, sam = 0.f;
   gate_partials(xs[0][0], xs[0][1], acc, saa, smm, sam);
 #pragma unroll
@@ -192,6 +206,10 @@ __global__ void __launch_bounds__(256, 2) lookup_bulk_kernel(const __grid_consta
   uint16_t *yrow = p.y + t * 4 * D + col0;
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
+    if (!EARLY && s > 0) {
+      xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
+      xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+    }
     const float c = g * __ldg(p.alpha + s);
     __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D), gated_add8(xs[s][0], acc, c));
     __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D + 8), gated_add8(xs[s][1], acc + 8, c));
@@ -207,13 +225,23 @@ __global__ void __launch_bounds__(256, 2) lookup_bulk_kernel(const __grid_consta
   }
 }
 
-template <int DT, bool AUX>
+template <int DT, bool AUX, bool EARLY>
 cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
-  auto kern = lookup_bulk_kernel<DT, AUX>;
+  auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)p.T, p.D / 16, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_bulk_dt(const LookupParams &p, size_t smem, bool aux, bool early,
+                           cudaStream_t stream) {
+  if (early)
+    return aux ? launch_bulk_t<DT, true, true>(p, smem, stream)
+               : launch_bulk_t<DT, false, true>(p, smem, stream);
+  return aux ? launch_bulk_t<DT, true, false>(p, smem, stream)
+             : launch_bulk_t<DT, false, false>(p, smem, stream);
 }
 
 }  // namespace
@@ -234,11 +262,12 @@ cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t st
   if (p.T == 0) return cudaSuccess;
   const size_t smem = bulk_smem_bytes(p.D, dtype, p.H);
   const bool aux = p.gate_out != nullptr || p.mem_out != nullptr;
+  // Four blocks per SM when four tokens' rows fit in shared memory (streams
+  // loaded after the rows); else two, with the streams loaded early.
+  const bool early = smem > 56 * 1024;
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
-    return aux ? launch_bulk_t<ENGRAM_TABLE_FP8_E4M3FN, true>(p, smem, stream)
-               : launch_bulk_t<ENGRAM_TABLE_FP8_E4M3FN, false>(p, smem, stream);
-  return aux ? launch_bulk_t<ENGRAM_TABLE_BF16, true>(p, smem, stream)
-             : launch_bulk_t<ENGRAM_TABLE_BF16, false>(p, smem, stream);
+    return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
+  return launch_bulk_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 
 }  // namespace engram
