@@ -176,7 +176,10 @@ def device_inputs(eg, cfg, rank, device):
     tabs, scales = W.tables_device(cfg, device)
     dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
     hist = W.history(cfg, rank)
+    pos, dead = W.packed_layout(cfg, rank) if cfg.packed else (None, None)
     return dict(
+        positions=None if pos is None else torch.from_numpy(pos).to(device),
+        dead=None if dead is None else torch.from_numpy(dead).to(device),
         ids=torch.from_numpy(W.token_ids(cfg, rank)).to(device),
         tid2eid=torch.from_numpy(W.tid2eid(cfg)).to(device),
         history=None if hist is None else torch.from_numpy(hist).to(device),
@@ -206,9 +209,10 @@ class Step:
         x = d["streams"] if x is None else x
         out = self.out if out is None else out
         eg.engram_compress(ids, d["tid2eid"], cfg.n_eids, eids_out=self.eids, status=self.status,
-                           stream=self.stream)
+                           stream=self.stream, dead=d["dead"])
         eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
-                       row_ids_out=self.rows, status=self.status, stream=self.stream)
+                       row_ids_out=self.rows, status=self.status, stream=self.stream,
+                       positions=d["positions"])
         if ev_start is not None:
             ev_start.record(self.stream)
         eg.engram_lookup_fused(self.rows, cfg.H, d["tables"], x, d["alpha"], cfg.eps,
@@ -275,12 +279,17 @@ def run_native(args):
     if clocks:
         clocks.stop()
 
-    e2e = None if args.no_e2e else run_e2e(eg, cfg, step, stream, args.e2e_steps, world, device)
+    # engram_forward_host takes no dead mask or positions: no e2e leg for packed batches
+    e2e = None if (args.no_e2e or cfg.packed) else run_e2e(eg, cfg, step, stream, args.e2e_steps,
+                                                           world, device)
     cpu = None if (args.no_cpu_baseline or rank != 0) else cpu_baseline(cfg, d, args.cpu_sample_tokens)
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
-        bytes_tok = cfg.algorithmic_bytes_per_token()
+        n_dead = int(d["dead"].sum().item()) if d["dead"] is not None else 0
+        # a dead token moves its row ids and a copy of its streams, no table rows
+        bytes_dead = cfg.R * 4 + 2 * 4 * cfg.D * 2
+        bytes_tok = (cfg.algorithmic_bytes_per_token() * (cfg.T - n_dead) + bytes_dead * n_dead) / cfg.T
         lk = statistics.mean(lookup_ms)
         achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
         traffic = recorded_traffic(cfg, args.lookup_kernel)
@@ -311,6 +320,7 @@ def run_native(args):
                 "frac": achieved / peak,
                 "traffic": traffic,
                 "algorithmic_bytes_per_token": bytes_tok,
+                "dead_tokens_per_step": n_dead,
                 "lookup_ms_mean": lk,
                 "lookup_ms_median": statistics.median(lookup_ms),
             },
@@ -390,23 +400,29 @@ def oracle_sample(cfg, d, n_tokens):
         hist = None
         x = d["streams"][:nseq].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
     tid2eid = d["tid2eid"].cpu().numpy()
-    e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
-    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist)
+    dead = None if d["dead"] is None else d["dead"][:ids.shape[0]].cpu().numpy()
+    pos = None if d["positions"] is None else d["positions"][:ids.shape[0]].cpu().numpy()
+    if dead is not None:
+        e, _ = oracle.compress_masked(ids, tid2eid, cfg.n_eids, dead)
+    else:
+        e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
+    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
     r = r.reshape(n, -1)
     # full-size host copies are too large: the oracle gets tables holding only the
     # rows the sample needs, with the row ids remapped onto them
     host_tabs, host_scales, remap = [], [], np.empty_like(r)
     for k in range(3):
         cols = slice(k * cfg.H, (k + 1) * cfg.H)
-        uniq, inv = np.unique(r[:, cols], return_inverse=True)
-        remap[:, cols] = inv.reshape(r[:, cols].shape)
+        live = r[:, cols] != oracle.DEAD
+        uniq, inv = np.unique(np.where(live, r[:, cols], 0), return_inverse=True)
+        remap[:, cols] = np.where(live, inv.reshape(r[:, cols].shape), oracle.DEAD)
         idx = torch.from_numpy(uniq.astype(np.int64)).to(d["tables"].tables[k].device)
         t = d["tables"].tables[k].index_select(0, idx).cpu().numpy()
         host_tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))
         host_scales.append(d["tables"].scales[k].index_select(0, idx).cpu().numpy()
                            if cfg.dtype == W.FP8 else None)
     return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=x, tables=host_tabs, scales=host_scales,
-                remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n)
+                remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n, dead=dead, positions=pos)
 
 
 def time_oracle(cfg, s, repeats=1):
@@ -414,8 +430,11 @@ def time_oracle(cfg, s, repeats=1):
     import oracle
     t0 = time.perf_counter()
     for _ in range(repeats):
-        e, _ = oracle.compress(s["ids"], s["tid2eid"], cfg.n_eids)
-        oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"])
+        if s.get("dead") is not None:
+            e, _ = oracle.compress_masked(s["ids"], s["tid2eid"], cfg.n_eids, s["dead"])
+        else:
+            e, _ = oracle.compress(s["ids"], s["tid2eid"], cfg.n_eids)
+        oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"], positions=s.get("positions"))
         oracle.lookup(s["remap"], cfg.H, oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16,
                       s["tables"], s["scales"], s["x"], s["alpha"], cfg.eps)
     return (time.perf_counter() - t0) / repeats
@@ -440,15 +459,20 @@ def reference_sample(cfg, n):
     ids = W.token_ids(sub)
     tid2eid = W.tid2eid(cfg)
     hist = W.history(sub)
-    e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
-    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist)
+    pos, dead = W.packed_layout(sub) if sub.packed else (None, None)
+    if dead is not None:
+        e, _ = oracle.compress_masked(ids, tid2eid, cfg.n_eids, dead)
+    else:
+        e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
+    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
     r = r.reshape(n, -1)
     g = np.random.default_rng([cfg.seed, 99])
     tabs, scs, remap = [], [], np.empty_like(r)
     for k in range(3):
         cols = slice(k * cfg.H, (k + 1) * cfg.H)
-        uniq, inv = np.unique(r[:, cols], return_inverse=True)
-        remap[:, cols] = inv.reshape(r[:, cols].shape)
+        live = r[:, cols] != oracle.DEAD
+        uniq, inv = np.unique(np.where(live, r[:, cols], 0), return_inverse=True)
+        remap[:, cols] = np.where(live, inv.reshape(r[:, cols].shape), oracle.DEAD)
         x = g.standard_normal((len(uniq), cfg.D), dtype=np.float32)
         if cfg.dtype == W.FP8:
             tabs.append(W._to_e4m3_bytes(x))
@@ -457,7 +481,8 @@ def reference_sample(cfg, n):
             tabs.append(W._to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scs.append(None)
     return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=W.streams_host(sub).reshape(n, 4, cfg.D),
-                tables=tabs, scales=scs, remap=remap, alpha=W.alpha(cfg), n=n)
+                tables=tabs, scales=scs, remap=remap, alpha=W.alpha(cfg), n=n, dead=dead,
+                positions=pos)
 
 
 def run_reference(args, budget_s: float = 60.0):

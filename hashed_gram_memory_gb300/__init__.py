@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libengram.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_TIMEOUT = range(6)
 FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
 TABLE_FP8_E4M3FN, TABLE_BF16 = 0, 1
+EID_DEAD = ROW_DEAD = -1
 LOOKUP_AUTO, LOOKUP_GATHER, LOOKUP_BULK = 0, 1, 2
 MAX_HEADS, MAX_D = 32, 4096
 
@@ -42,11 +43,15 @@ def _load():
     L = C.CDLL(LIB_PATH)
     vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
     L.engram_compress.argtypes = [vp, i64, vp, i32, i32, vp, vp, vp]
+    L.engram_compress_masked.argtypes = [vp, i64, vp, i32, i32, vp, vp, vp, vp]
     L.engram_hash.argtypes = [vp, i32, i32, vp, vp, i32, C.POINTER(C.c_int64), vp, vp, vp]
+    L.engram_hash_packed.argtypes = [vp, i32, i32, vp, vp, vp, i32, C.POINTER(C.c_int64), vp, vp,
+                                     vp]
     L.engram_lookup_fused.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, vp, vp,
                                       C.c_float, vp, vp, vp, vp]
     L.engram_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
-    for f in ("engram_compress", "engram_hash", "engram_lookup_fused", "engram_read_status"):
+    for f in ("engram_compress", "engram_compress_masked", "engram_hash", "engram_hash_packed",
+              "engram_lookup_fused", "engram_read_status"):
         getattr(L, f).restype = C.c_int32
     L.engram_status_string.argtypes = [C.c_int32]
     L.engram_status_string.restype = C.c_char_p
@@ -138,23 +143,28 @@ class Tables:
         return s
 
 
-def engram_compress(token_ids, tid2eid, n_eids: int, eids_out=None, status=None, stream=None):
-    """eids_out[i] = tid2eid[token_ids[i]] (int32, same shape as token_ids)."""
+def engram_compress(token_ids, tid2eid, n_eids: int, eids_out=None, status=None, stream=None,
+                    dead=None):
+    """eids_out[i] = tid2eid[token_ids[i]] (int32, same shape as token_ids); with a
+    dead mask (uint8/bool, same shape) dead positions become EID_DEAD."""
     import torch
     _need(token_ids, (torch.int32,), "token_ids")
     _need(tid2eid, (torch.int32,), "tid2eid")
+    _need(dead, (torch.uint8, torch.bool), "dead")
     if eids_out is None:
         eids_out = torch.empty_like(token_ids)
     _need(eids_out, (torch.int32,), "eids_out")
-    _check(lib.engram_compress(_ptr(token_ids), token_ids.numel(), _ptr(tid2eid), tid2eid.numel(),
-                               n_eids, _ptr(eids_out), _ptr(status), _stream(stream)),
+    _check(lib.engram_compress_masked(_ptr(token_ids), token_ids.numel(), _ptr(tid2eid),
+                                      tid2eid.numel(), n_eids, _ptr(dead), _ptr(eids_out),
+                                      _ptr(status), _stream(stream)),
            "engram_compress")
     return eids_out
 
 
 def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_ids_out=None,
-                status=None, stream=None):
-    """Row ids [B, S, 3, n_heads] int32 for eids [B, S]; history/history_out [B, 3]."""
+                status=None, stream=None, positions=None):
+    """Row ids [B, S, 3, n_heads] int32 for eids [B, S]; history/history_out [B, 3];
+    positions [B, S] (optional): each token's index within its packed sample."""
     import torch
     _need(eids, (torch.int32,), "eids")
     if eids.dim() != 2:
@@ -165,9 +175,11 @@ def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_id
     _need(row_ids_out, (torch.int32,), "row_ids_out")
     _need(history, (torch.int32,), "history")
     _need(history_out, (torch.int32,), "history_out")
+    _need(positions, (torch.int32,), "positions")
     r = (C.c_int64 * 3)(*[int(x) for x in rows])
-    _check(lib.engram_hash(_ptr(eids), B, S, _ptr(history), _ptr(history_out), n_heads, r,
-                           _ptr(row_ids_out), _ptr(status), _stream(stream)), "engram_hash")
+    _check(lib.engram_hash_packed(_ptr(eids), B, S, _ptr(positions), _ptr(history),
+                                  _ptr(history_out), n_heads, r, _ptr(row_ids_out), _ptr(status),
+                                  _stream(stream)), "engram_hash")
     return row_ids_out
 
 

@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   uint32_t flags = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += stride) {
+    if (p.dead && p.dead[i]) {
+      p.eids_out[i] = ENGRAM_EID_DEAD;
+      continue;
+    }
     const int32_t tok = p.token_ids[i];
     if ((uint32_t)tok >= (uint32_t)p.vocab) {
       flags |= ENGRAM_FLAG_BAD_TOKEN;
@@ -49,8 +53,10 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
 }
 
 // One thread per (token, order, head).  Thread r of a token computes row id r
-// (n-major: r = (n-2)*H + j) from the token's 4-id window s-3 .. s, taking ids
-// before position 0 from the history (or the pad id 0).
+// (n-major: r = (n-2)*H + j) from the token's window, read back from the token
+// until its lookback limit (its position in its sample if positions are given,
+// else 3 with a history and s without) or a dead id, whichever comes first;
+// the slots beyond hold the pad id 0.  A dead token writes ENGRAM_ROW_DEAD.
 __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashParams p) {
   const int R = 3 * p.H;
   const int tl = threadIdx.x / R;
@@ -58,24 +64,47 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
   const int64_t t = (int64_t)blockIdx.x * p.tokens_per_block + tl;
   const bool valid = tl < p.tokens_per_block && t < p.T;
   uint32_t flags = 0;
-  int32_t w[4] = {0, 0, 0, 0};
+  int32_t w[4] = {0, 0, 0, 0};  // oldest first, w[3] = the token's own id
+  int32_t raw[4] = {0, 0, 0, 0};  // the ids s-3 .. s as stored (for history_out)
   int b = 0;
   if (valid) {
     b = (int)(t / p.seq);
     const int s = (int)(t - (int64_t)b * p.seq);
-    bool ok = true;
+    const int64_t base = (int64_t)b * p.seq;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int pos = s - 3 + k;
-      int32_t e = 0;
       if (pos >= 0)
-        e = __ldg(p.eids + (int64_t)b * p.seq + pos);
+        raw[k] = __ldg(p.eids + base + pos);
       else if (p.history)
-        e = p.history[(int64_t)b * 3 + 3 + pos];  // plain load: history may be rewritten below
-      w[k] = e;
-      ok &= (e >= 0);
+        raw[k] = p.history[(int64_t)b * 3 + 3 + pos];  // plain load: history may be rewritten below
     }
-    if (ok) {
+    const int32_t self = raw[3];
+    bool dead = self == ENGRAM_EID_DEAD, bad = self < ENGRAM_EID_DEAD;
+    if (!dead && !bad) {
+      w[3] = self;
+      const int64_t limit = p.positions ? (int64_t)p.positions[base + s] : (p.history ? 3 : s);
+      bool blocked = false;
+#pragma unroll
+      for (int k = 1; k <= 3; ++k) {
+        int32_t e = 0;
+        if (!blocked && k <= limit && (s - k >= 0 || p.history)) {
+          e = raw[3 - k];
+          if (e == ENGRAM_EID_DEAD) {
+            blocked = true;
+            e = 0;
+          } else if (e < 0) {
+            bad = true;
+          }
+        }
+        w[3 - k] = e;
+      }
+    }
+    if (bad) {
+      flags = ENGRAM_FLAG_BAD_EID;
+    } else if (dead) {
+      p.row_ids[t * R + r] = ENGRAM_ROW_DEAD;
+    } else {
       const int ni = (r >= p.H) + (r >= 2 * p.H);  // n - 2
       const int j = r - ni * p.H;
       uint64_t h = p.seed[ni][j];
@@ -87,8 +116,6 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
         }
       }
       p.row_ids[t * R + r] = (int32_t)mod_by_reciprocal(h, p.rows[ni], p.rmul[ni]);
-    } else {
-      flags = ENGRAM_FLAG_BAD_EID;
     }
   }
   flag_warp(p.status, flags);
@@ -97,7 +124,7 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
     __syncthreads();
     if (valid && r == 0) {
 #pragma unroll
-      for (int k = 0; k < 3; ++k) p.history_out[(int64_t)b * 3 + k] = w[k + 1];
+      for (int k = 0; k < 3; ++k) p.history_out[(int64_t)b * 3 + k] = raw[k + 1];
     }
   }
 }

@@ -100,9 +100,11 @@ ENGRAM_API const char *engram_status_string(engram_status code) {
   }
 }
 
-ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tokens,
-                                         const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
-                                         int32_t *eids_out, int32_t *status, void *stream) {
+ENGRAM_API engram_status engram_compress_masked(const int32_t *token_ids, int64_t n_tokens,
+                                                const int32_t *tid2eid, int32_t vocab,
+                                                int32_t n_eids, const uint8_t *dead,
+                                                int32_t *eids_out, int32_t *status,
+                                                void *stream) {
   if (n_tokens < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_tokens < 0");
   if (vocab < 1) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: vocab < 1");
   if (n_eids < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_eids < 0");
@@ -115,17 +117,27 @@ ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tok
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: token_ids and eids_out overlap partially");
   if (overlap(tid2eid, (size_t)vocab * 4, eids_out, n_tokens * 4))
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: eids_out overlaps tid2eid");
+  if (dead && overlap(dead, n_tokens, eids_out, n_tokens * 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: eids_out overlaps the dead mask");
   if (n_tokens == 0) return ok();
   engram_status st = check_device();
   if (st != ENGRAM_OK) return st;
-  engram::CompressParams p{token_ids, n_tokens, tid2eid, vocab, n_eids, eids_out, status};
+  engram::CompressParams p{token_ids, n_tokens, dead, tid2eid, vocab, n_eids, eids_out, status};
   return launched("engram_compress launch", engram::launch_compress(p, (cudaStream_t)stream));
 }
 
-ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,
-                                     const int32_t *history, int32_t *history_out,
-                                     int32_t n_heads, const int64_t *rows_host,
-                                     int32_t *row_ids_out, int32_t *status, void *stream) {
+ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tokens,
+                                         const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
+                                         int32_t *eids_out, int32_t *status, void *stream) {
+  return engram_compress_masked(token_ids, n_tokens, tid2eid, vocab, n_eids, nullptr, eids_out,
+                                status, stream);
+}
+
+ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, int32_t seq,
+                                            const int32_t *positions, const int32_t *history,
+                                            int32_t *history_out, int32_t n_heads,
+                                            const int64_t *rows_host, int32_t *row_ids_out,
+                                            int32_t *status, void *stream) {
   if (batch < 0 || seq < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: batch or seq < 0");
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: n_heads must be in [1, %d]", ENGRAM_MAX_HEADS);
@@ -151,12 +163,16 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
   }
   if (history && overlap(history, (size_t)batch * 12, row_ids_out, T * R * 4))
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: row_ids_out overlaps history");
+  if (positions && (!aligned(positions, 4) || overlap(positions, T * 4, row_ids_out, T * R * 4) ||
+                    (history_out && overlap(positions, T * 4, history_out, (size_t)batch * 12))))
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: positions misaligned or overlapping outputs");
   if (T == 0 && (!history_out || batch == 0)) return ok();
   engram_status st = check_device();
   if (st != ENGRAM_OK) return st;
   engram::HashParams p;
   memset(&p, 0, sizeof p);
   p.eids = eids;
+  p.positions = positions;
   p.history = history;
   p.history_out = history_out;
   p.row_ids = row_ids_out;
@@ -171,6 +187,14 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
     for (int j = 0; j < n_heads; ++j) p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
   }
   return launched("engram_hash launch", engram::launch_hash(p, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,
+                                     const int32_t *history, int32_t *history_out,
+                                     int32_t n_heads, const int64_t *rows_host,
+                                     int32_t *row_ids_out, int32_t *status, void *stream) {
+  return engram_hash_packed(eids, batch, seq, nullptr, history, history_out, n_heads, rows_host,
+                            row_ids_out, status, stream);
 }
 
 ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,

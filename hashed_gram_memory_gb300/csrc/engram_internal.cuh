@@ -16,6 +16,7 @@ constexpr int kMaxRows = 3 * kMaxHeads;
 struct CompressParams {
   const int32_t *token_ids;
   int64_t n;
+  const uint8_t *dead;  // optional: dead positions become ENGRAM_EID_DEAD
   const int32_t *tid2eid;
   int32_t vocab;
   int32_t n_eids;
@@ -25,6 +26,7 @@ struct CompressParams {
 
 struct HashParams {
   const int32_t *eids;
+  const int32_t *positions;  // optional: index of each token within its sample
   const int32_t *history;
   int32_t *history_out;
   int32_t *row_ids;

@@ -19,7 +19,7 @@
 // block set ENGRAM_FLAG_TIMEOUT, skip the token, and exit only after thread 0
 // has waited (again bounded) for the copies it issued.  An id outside its table
 // makes the block set ENGRAM_FLAG_BAD_ROW and skip the token before anything
-// is copied.
+// is copied; a dead token (all ids ENGRAM_ROW_DEAD) copies its streams through.
 #include "engram_internal.cuh"
 #include "lookup_common.cuh"
 
@@ -106,15 +106,27 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // Range checks: thread r looks at row r (a loop when the block is narrower).
-  bool bad_here = false;
+  bool bad_here = false, dead_here = false, live_here = false;
   for (int r = tid; r < R; r += blockDim.x) {
     const int ni = (r >= H) + (r >= 2 * H);
     const int32_t id = ids[r];
-    bad_here |= (id < 0) | ((int64_t)id >= p.rows[ni]);
+    if (id == ENGRAM_ROW_DEAD) {
+      dead_here = true;
+    } else {
+      live_here = true;
+      bad_here |= (id < 0) | ((int64_t)id >= p.rows[ni]);
+    }
   }
-  if (__syncthreads_or(bad_here)) {
-    if (tid == 0 && p.status) atomicOr(p.status, ENGRAM_FLAG_BAD_ROW);
-    return;  // whole block: nothing issued, nothing written
+  if (__syncthreads_or(bad_here || dead_here)) {
+    // A token whose ids are all dead passes through; any other mix is bad.
+    if (__syncthreads_and(!live_here)) {
+      pass_through16(p.x + t * 4 * D + col0, p.y + t * 4 * D + col0, D,
+                     AUX && p.gate_out ? p.gate_out + t : nullptr,
+                     AUX && p.mem_out ? p.mem_out + t * D + col0 : nullptr, tid == 0);
+    } else if (tid == 0 && p.status) {
+      atomicOr(p.status, ENGRAM_FLAG_BAD_ROW);
+    }
+    return;  // whole block: nothing issued
   }
 
   // Thread 0: every row copy of the token on the one barrier.

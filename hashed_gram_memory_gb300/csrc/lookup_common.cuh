@@ -79,4 +79,25 @@ __device__ __forceinline__ uint4 gated_add8(const uint4 &in, const float *m, flo
   return out;
 }
 
+// A dead token's four stream slices (16 columns each) copied through unchanged
+// (nothing to do in place); its gate and memory outputs are zero.
+__device__ __forceinline__ void pass_through16(const uint16_t *xrow, uint16_t *yrow, int D,
+                                               float *gate_out, float *mem_row, bool lead) {
+  if (yrow != xrow) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
+      const uint4 b = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+      __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D), a);
+      __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D + 8), b);
+    }
+  }
+  if (gate_out && lead) *gate_out = 0.f;
+  if (mem_row) {
+    float4 *mo = reinterpret_cast<float4 *>(mem_row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mo[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 }  // namespace engram

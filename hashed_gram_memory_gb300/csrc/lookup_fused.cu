@@ -56,15 +56,21 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
   const int col0 = lane_t * 16;
   const int32_t *ids = s_ids + tl * R;
   bool bad = false;
+  int ndead = 0;
   if (tok_valid) {
     for (int r = 0; r < R; ++r) {
       const int ni = (r >= H) + (r >= 2 * H);
       const int32_t id = ids[r];
-      bad |= (id < 0) | ((int64_t)id >= p.rows[ni]);
+      if (id == ENGRAM_ROW_DEAD)
+        ++ndead;
+      else
+        bad |= (id < 0) | ((int64_t)id >= p.rows[ni]);
     }
+    bad |= ndead > 0 && ndead < R;  // some dead, some live
     if (bad && lane_t == 0 && p.status) atomicOr(p.status, ENGRAM_FLAG_BAD_ROW);
   }
-  const bool work = tok_valid && !bad && col0 < p.D;
+  const bool dead = tok_valid && !bad && ndead == R;
+  const bool work = tok_valid && !bad && !dead && col0 < p.D;
 
   // The token's four stream slices, loaded first: stream 0 feeds the gate and
   // all four are rewritten at the end.
@@ -144,7 +150,13 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
     }
   }
 
-  if (!work) return;
+  if (!work) {
+    if (dead && col0 < p.D)
+      pass_through16(p.x + t * 4 * p.D + col0, p.y + t * 4 * p.D + col0, p.D,
+                     AUX && p.gate_out ? p.gate_out + t : nullptr,
+                     AUX && p.mem_out ? p.mem_out + t * p.D + col0 : nullptr, lane_t == 0);
+    return;
+  }
 
   const float g = gate_value(saa, smm, sam, (float)p.D, p.eps, p.sqrt_D);
 

@@ -77,6 +77,18 @@ typedef int32_t engram_status;
 #define ENGRAM_TABLE_BF16 1
 
 /*
+ * Dead positions (image spans: vLLM page, DeepseekV4Model.forward, they break
+ * n-grams and their gate is zeroed; VeOmni PR page, pack_ngram_inputs commit,
+ * a blocked lookback compresses to pad): a dead position's compressed id is
+ * ENGRAM_EID_DEAD; an n-gram never spans it (the ids at and before it read as
+ * the pad id 0, as before a sequence start); the dead token's own 3H row ids
+ * are ENGRAM_ROW_DEAD, and engram_lookup_fused passes such a token's streams
+ * through unchanged (g = 0).
+ */
+#define ENGRAM_EID_DEAD (-1)
+#define ENGRAM_ROW_DEAD (-1)
+
+/*
  * The three n-gram tables (index 0, 1, 2 = orders 2, 3, 4), row-major
  * [rows[n], D], each 16-byte aligned.  FP8: one byte per element (OCP E4M3,
  * "fn": bias 7, max 448, no infinities) and scale[n] = fp32 [rows[n]], the
@@ -110,12 +122,23 @@ ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tok
                                          int32_t *eids_out, int32_t *status, void *stream);
 
 /*
+ * engram_compress_masked -- engram_compress with a dead mask: dead[i] != 0
+ * (uint8 [n_tokens], device) makes eids_out[i] = ENGRAM_EID_DEAD whatever the
+ * token id (no range check for it); dead may be NULL (then as engram_compress).
+ */
+ENGRAM_API engram_status engram_compress_masked(const int32_t *token_ids, int64_t n_tokens,
+                                                const int32_t *tid2eid, int32_t vocab,
+                                                int32_t n_eids, const uint8_t *dead,
+                                                int32_t *eids_out, int32_t *status,
+                                                void *stream);
+
+/*
  * engram_hash -- n-gram hash ids per order and head (VeOmni PR page, commit
  * "n-gram memory lookup" and the commit on the incremental decode cache: a
  * window never reaches past position 0; a three-id tail of history is the whole
  * cache and is exact; NeMo AutoModel page: engram_hash_ids [batch, sequence,
  * hash_heads]).
- *   eids        int32 [batch, seq] compressed ids (>= 0)
+ *   eids        int32 [batch, seq] compressed ids (>= 0, or ENGRAM_EID_DEAD)
  *   history     int32 [batch, 3] or NULL: the three ids before position 0,
  *               oldest first; NULL means every sequence starts here (positions
  *               before 0 are the pad id 0)
@@ -126,14 +149,34 @@ ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tok
  *   rows_host   host int64 [3]: rows of the 2-, 3-, 4-gram tables, 1..2^31-1
  *   row_ids_out int32 [batch, seq, 3, n_heads], n-major: the row for order n,
  *               head j of token (b, s) is at ((b*seq + s)*3 + n-2)*n_heads + j
- * The window of order n at (b, s) is ids s-n+1 .. s.  A negative id in
- * positions s-3 .. s sets ENGRAM_FLAG_BAD_EID and leaves that token's 3*n_heads
- * ids unwritten.  1 <= n_heads <= ENGRAM_MAX_HEADS.
+ * The window of order n at (b, s) is ids s-n+1 .. s, read back from s until
+ * the lookback limit (s without a history, 3 with one) or a dead id, whichever
+ * comes first; the slots beyond read as the pad id 0.  A dead token gets
+ * ENGRAM_ROW_DEAD for all its ids.  A read id below ENGRAM_EID_DEAD sets
+ * ENGRAM_FLAG_BAD_EID and leaves that token's 3*n_heads ids unwritten.
+ * history_out carries dead ids like any other.  1 <= n_heads <= ENGRAM_MAX_HEADS.
  */
 ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,
                                      const int32_t *history, int32_t *history_out,
                                      int32_t n_heads, const int64_t *rows_host,
                                      int32_t *row_ids_out, int32_t *status, void *stream);
+
+/*
+ * engram_hash_packed -- engram_hash for packed batches and resumed sequences:
+ * positions (int32 [batch, seq], device; may be NULL) gives every token's index
+ * within its own sample, restarting at 0 where a new sample starts (VeOmni PR
+ * page, review of pack_ngram_inputs: n-gram hashes never cross sample
+ * boundaries in a packed micro-batch).  The lookback limit of (b, s) is
+ * positions[b, s]: a window never reaches before its sample's start, in the
+ * batch or in the history (decode cache commit: the history sets how far back
+ * the walk can read, the start position whether it reached the true start).
+ * NULL positions is engram_hash.
+ */
+ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, int32_t seq,
+                                            const int32_t *positions, const int32_t *history,
+                                            int32_t *history_out, int32_t n_heads,
+                                            const int64_t *rows_host, int32_t *row_ids_out,
+                                            int32_t *status, void *stream);
 
 /*
  * engram_lookup_fused -- gather + dequantise the 3*n_heads rows of every token,
@@ -152,7 +195,10 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
  *   gate_out    fp32 [n_tokens] or NULL: g per token
  *   mem_out     fp32 [n_tokens, D] or NULL (16-byte aligned): m per token
  * A row id outside its table sets ENGRAM_FLAG_BAD_ROW and leaves the token's
- * outputs unwritten.
+ * outputs unwritten.  A token whose 3*n_heads ids are all ENGRAM_ROW_DEAD is a
+ * dead token: nothing is gathered, its streams are copied through unchanged
+ * (nothing is written in place), g = 0 and m = 0; some dead and some live ids
+ * is a bad row.
  */
 ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
                                              int32_t n_heads, const engram_tables *tables_host,
@@ -284,7 +330,7 @@ ENGRAM_API const char *engram_status_string(engram_status code);
 ENGRAM_API const char *engram_last_error(void);
 
 /* ABI version of this header (incremented on any incompatible change). */
-#define ENGRAM_ABI_VERSION 1
+#define ENGRAM_ABI_VERSION 2
 ENGRAM_API int32_t engram_abi_version(void);
 
 #ifdef __cplusplus

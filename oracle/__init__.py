@@ -16,6 +16,7 @@ from . import build as _build
 
 FP8 = 0
 BF16 = 1
+DEAD = -1
 BAD_TOKEN, BAD_EID, BAD_ROW, BAD_ARG = 1, 2, 4, 16
 
 _lib = None
@@ -42,6 +43,12 @@ def lib():
         L.orc_compress.restype = C.c_int
         L.orc_compress.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int32, C.c_int32,
                                    C.c_void_p]
+        L.orc_compress_masked.restype = C.c_int
+        L.orc_compress_masked.argtypes = [C.c_void_p, C.c_int64, C.c_void_p, C.c_int32, C.c_int32,
+                                          C.c_void_p, C.c_void_p]
+        L.orc_hash_packed.restype = C.c_int
+        L.orc_hash_packed.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                      C.c_int32, C.POINTER(C.c_int64), C.c_void_p, C.c_void_p]
         L.orc_hash.restype = C.c_int
         L.orc_hash.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int32,
                                C.POINTER(C.c_int64), C.c_void_p, C.c_void_p]
@@ -102,17 +109,30 @@ def compress(token_ids, tid2eid, n_eids: int, fill: int = -7):
     return out, int(flags)
 
 
+def compress_masked(token_ids, tid2eid, n_eids: int, dead, fill: int = -7):
+    """As compress, with dead positions (mask != 0) set to DEAD."""
+    tid = _c(token_ids, np.int32)
+    m = _c(tid2eid, np.int32)
+    d = _c(dead, np.uint8)
+    assert d.shape == tid.shape
+    out = np.full(tid.shape, fill, dtype=np.int32)
+    flags = lib().orc_compress_masked(_p(tid), tid.size, _p(m), m.size, n_eids, _p(d), _p(out))
+    return out, int(flags)
+
+
 def hash_ids(eids, n_heads: int, rows, history=None, want_history: bool = False,
-             fill: int = -7):
-    """Row ids [B, S, 3, H] (and the next history [B, 3]) and the error flags."""
+             fill: int = -7, positions=None):
+    """Row ids [B, S, 3, H] (and the next history [B, 3]) and the error flags.
+    positions [B, S] (optional): each token's index within its packed sample."""
     e = _c(eids, np.int32)
     assert e.ndim == 2
     B, S = e.shape
     hist = None if history is None else _c(history, np.int32).reshape(B, 3)
+    pos = None if positions is None else _c(positions, np.int32).reshape(B, S)
     out = np.full((B, S, 3, n_heads), fill, dtype=np.int32)
     hout = np.full((B, 3), fill, dtype=np.int32) if want_history else None
     r = (C.c_int64 * 3)(*[int(x) for x in rows])
-    flags = lib().orc_hash(_p(e), B, S, _p(hist), n_heads, r, _p(out), _p(hout))
+    flags = lib().orc_hash_packed(_p(e), B, S, _p(pos), _p(hist), n_heads, r, _p(out), _p(hout))
     if want_history:
         return out, hout, int(flags)
     return out, int(flags)

@@ -129,6 +129,26 @@ int orc_compress(const int32_t *token_ids, int64_t n, const int32_t *tid2eid, in
 }
 
 /*
+ * tid2eid compression with a dead mask: a dead position (an image span, P3:
+ * image-span tokens are dead and break n-grams; P1 pack_ngram_inputs commit: they
+ * reach compression marked dead) becomes ORC_DEAD whatever its token id; the
+ * others as orc_compress.
+ */
+int orc_compress_masked(const int32_t *token_ids, int64_t n, const int32_t *tid2eid,
+                        int32_t vocab, int32_t n_eids, const uint8_t *dead, int32_t *eids_out) {
+  int flags = 0;
+  if (n < 0 || vocab < 1 || n_eids < 0) return ORC_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    if (dead && dead[i]) {
+      eids_out[i] = ORC_DEAD;
+      continue;
+    }
+    flags |= orc_compress(token_ids + i, 1, tid2eid, vocab, n_eids, eids_out + i);
+  }
+  return flags;
+}
+
+/*
  * The compressed id at position p of sequence b.  Positions before the start of
  * the call take the caller's history (the last three ids of the earlier
  * sequence, oldest first) when one is given, else the pad id 0: an n-gram never
@@ -144,18 +164,58 @@ static int32_t orc_eid_at(const int32_t *eids, int32_t S, const int32_t *history
 }
 
 /*
+ * The 4-id window of token (b, s), oldest first (w4[3] is the token's own id),
+ * with lookback blocking (VeOmni PR page, "n-gram memory lookup" commit: an
+ * n-gram never spans an image span or reaches past position 0; the commit on
+ * pack_ngram_inputs: a blocked lookback compresses to pad; the review on packed
+ * batches: positions restart at 0 per sample and bound the lookback; the decode
+ * cache commit: history sets how far back the walk can read, the start position
+ * whether it has reached the true start).  The id k back (k = 1..3) is read only
+ * if k <= limit, where limit = positions[b, s] when positions are given, else 3
+ * with a history and s without, and only if no id 1..k back is ORC_DEAD; every
+ * other slot is the pad id 0.
+ * Returns 0, 1 when the token itself is dead, or ORC_BAD_EID for a read id
+ * below ORC_DEAD.
+ */
+static int orc_window(const int32_t *eids, int32_t S, const int32_t *positions,
+                      const int32_t *history, int32_t b, int32_t s, int32_t w4[4]) {
+  const int32_t self = eids[(int64_t)b * S + s];
+  if (self == ORC_DEAD) return 1;
+  if (self < 0) return ORC_BAD_EID;
+  w4[3] = self;
+  int64_t limit = positions ? positions[(int64_t)b * S + s] : (history ? 3 : s);
+  int blocked = 0;
+  for (int k = 1; k <= 3; ++k) {
+    int32_t e = 0;
+    if (!blocked && k <= limit && (s - k >= 0 || history)) {
+      e = orc_eid_at(eids, S, history, b, s - k);
+      if (e == ORC_DEAD) {
+        blocked = 1;
+        e = 0;
+      } else if (e < 0) {
+        return ORC_BAD_EID;
+      }
+    }
+    w4[3 - k] = e;
+  }
+  return 0;
+}
+
+/*
  * Hash ids [B, S, 3, H] (n-major: index ((b*S + s)*3 + (n-2))*H + j) for the
  * 2-, 3- and 4-gram ending at every position (NeMo AutoModel page,
- * DeepseekV41Block.forward: engram_hash_ids [batch, sequence, hash_heads]).  The
- * window of order n at position s is the ids at s-n+1 .. s, oldest first.
- * row = h mod rows_n, unsigned, on the full 64-bit h.  A negative id anywhere in
- * the 4-id window s-3 .. s leaves all 3H ids of that token unwritten and sets a
- * flag.  history_out (optional) receives the last three ids of history ++ eids,
- * oldest first: the next call's history.
+ * DeepseekV41Block.forward: engram_hash_ids [batch, sequence, hash_heads]), with
+ * positions (may be NULL) giving each token's index within its packed sample.
+ * The window of order n is the last n ids of the token's blocked window.  row =
+ * h mod rows_n, unsigned, on the full 64-bit h.  A dead token gets ORC_DEAD for
+ * all its 3H ids.  A read id below ORC_DEAD leaves all 3H ids of that token
+ * unwritten and sets a flag.  history_out (optional) receives the last three
+ * ids of history ++ eids, oldest first, dead ones included: the next call's
+ * history.
  */
-int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
-             int32_t n_heads, const int64_t rows[3], int32_t *row_ids_out,
-             int32_t *history_out) {
+int orc_hash_packed(const int32_t *eids, int32_t B, int32_t S, const int32_t *positions,
+                    const int32_t *history, int32_t n_heads, const int64_t rows[3],
+                    int32_t *row_ids_out, int32_t *history_out) {
   if (B < 0 || S < 0 || n_heads < 1) return ORC_BAD_ARG;
   for (int n = 0; n < 3; ++n)
     if (rows[n] < 1) return ORC_BAD_ARG;
@@ -166,21 +226,19 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
   for (int64_t t = 0; t < T; ++t) {
     int32_t b = (int32_t)(t / S), s = (int32_t)(t % S);
     int32_t w4[4];
-    int bad = 0;
-    for (int k = 0; k < 4; ++k) {
-      w4[k] = orc_eid_at(eids, S, history, b, s - 3 + k);
-      if (w4[k] < 0) bad = 1;
-    }
-    if (bad) {
+    int st = orc_window(eids, S, positions, history, b, s, w4);
+    if (st == ORC_BAD_EID) {
       flags |= ORC_BAD_EID;
       continue;
     }
-    for (int n = 2; n <= 4; ++n) {
-      const int32_t *window = w4 + (4 - n); /* ids at s-n+1 .. s */
-      for (int j = 0; j < n_heads; ++j) {
-        uint64_t h = orc_ngram_hash(window, n, j);
-        row_ids_out[t * R + (int64_t)(n - 2) * n_heads + j] = (int32_t)(h % (uint64_t)rows[n - 2]);
+    for (int r = 0; r < R; ++r) {
+      int n = 2 + r / n_heads, j = r % n_heads;
+      if (st == 1) {
+        row_ids_out[t * R + r] = ORC_DEAD;
+        continue;
       }
+      uint64_t h = orc_ngram_hash(w4 + (4 - n), n, j); /* ids at s-n+1 .. s */
+      row_ids_out[t * R + r] = (int32_t)(h % (uint64_t)rows[n - 2]);
     }
   }
   if (history_out) {
@@ -191,6 +249,14 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
     }
   }
   return flags;
+}
+
+/* orc_hash_packed with every sequence starting at position 0 of its sample
+ * (or continuing its history). */
+int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
+             int32_t n_heads, const int64_t rows[3], int32_t *row_ids_out,
+             int32_t *history_out) {
+  return orc_hash_packed(eids, B, S, NULL, history, n_heads, rows, row_ids_out, history_out);
 }
 
 /*
@@ -207,7 +273,9 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
  *     streams before its layer; NeMo AutoModel page: streams [batch, sequence,
  *     streams, hidden]).
  * A row id outside [0, rows_n) leaves the token's outputs unwritten and sets a
- * flag.  gate_out [n_tokens] and mem_out [n_tokens, D] are optional.
+ * flag; a token whose 3H ids are all ORC_DEAD passes through with g = 0 and
+ * m = 0 (some but not all dead is a bad row).  gate_out [n_tokens] and mem_out
+ * [n_tokens, D] are optional.
  */
 int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
                int32_t D, const void *const tables[3], const float *const scales[3],
@@ -220,13 +288,27 @@ int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : flags)
   for (int64_t t = 0; t < n_tokens; ++t) {
     const int32_t *ids = row_ids + t * R;
-    int bad = 0;
+    int bad = 0, dead = 0;
     for (int r = 0; r < R; ++r) {
       int n = r / n_heads;
-      if (ids[r] < 0 || (int64_t)ids[r] >= rows[n]) bad = 1;
+      if (ids[r] == ORC_DEAD)
+        ++dead;
+      else if (ids[r] < 0 || (int64_t)ids[r] >= rows[n])
+        bad = 1;
     }
-    if (bad) {
+    if (bad || (dead && dead != R)) {
       flags |= ORC_BAD_ROW;
+      continue;
+    }
+    if (dead) {
+      /* A dead token's gate is zeroed (vLLM page, DeepseekV4Model.forward: the
+       * Engram mask keeps live tokens only): its streams pass through unchanged. */
+      const uint16_t *xd = streams_in + t * 4 * (int64_t)D;
+      uint16_t *yd = streams_out + t * 4 * (int64_t)D;
+      if (yd != xd) memcpy(yd, xd, (size_t)4 * D * sizeof(uint16_t));
+      if (gate_out) gate_out[t] = 0.0;
+      if (mem_out)
+        for (int i = 0; i < D; ++i) mem_out[t * D + i] = 0.0;
       continue;
     }
     double *m = (double *)calloc((size_t)D, sizeof(double));

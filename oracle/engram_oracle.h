@@ -34,6 +34,10 @@ extern "C" {
 #define ORC_FP8_E4M3FN 0
 #define ORC_BF16 1
 
+/* A dead position (an image span): compresses to this marker, blocks every
+ * n-gram that would span it, and its token's row ids are all ORC_DEAD. */
+#define ORC_DEAD (-1)
+
 uint64_t orc_splitmix64(uint64_t x);
 uint64_t orc_seed(int n, int j);
 uint64_t orc_ngram_hash(const int32_t *window, int n, int j);
@@ -44,9 +48,16 @@ uint16_t orc_bf16_round(double y);
 int orc_compress(const int32_t *token_ids, int64_t n, const int32_t *tid2eid, int32_t vocab,
                  int32_t n_eids, int32_t *eids_out);
 
+int orc_compress_masked(const int32_t *token_ids, int64_t n, const int32_t *tid2eid,
+                        int32_t vocab, int32_t n_eids, const uint8_t *dead, int32_t *eids_out);
+
 int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
              int32_t n_heads, const int64_t rows[3], int32_t *row_ids_out,
              int32_t *history_out);
+
+int orc_hash_packed(const int32_t *eids, int32_t B, int32_t S, const int32_t *positions,
+                    const int32_t *history, int32_t n_heads, const int64_t rows[3],
+                    int32_t *row_ids_out, int32_t *history_out);
 
 int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
                int32_t D, const void *const tables[3], const float *const scales[3],

@@ -34,18 +34,25 @@ class HostInputs:
     scales: list
     streams: np.ndarray
     alpha: np.ndarray
+    positions: np.ndarray | None = None   # packed samples: index within the sample
+    dead: np.ndarray | None = None        # packed samples: image-span positions
 
 
 def host_inputs(cfg: W.EngramConfig, rank: int = 0) -> HostInputs:
     tabs, scales = W.tables_host(cfg)
+    pos, dead = W.packed_layout(cfg, rank) if cfg.packed else (None, None)
     return HostInputs(cfg, W.token_ids(cfg, rank), W.tid2eid(cfg), W.history(cfg, rank), tabs,
-                      scales, W.streams_host(cfg, rank), W.alpha(cfg))
+                      scales, W.streams_host(cfg, rank), W.alpha(cfg), pos, dead)
 
 
 def oracle_path(inp: HostInputs):
     cfg = inp.cfg
-    eids, f1 = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
-    rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history, want_history=True)
+    if inp.dead is not None:
+        eids, f1 = oracle.compress_masked(inp.ids, inp.tid2eid, cfg.n_eids, inp.dead)
+    else:
+        eids, f1 = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
+    rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history, want_history=True,
+                                     positions=inp.positions)
     y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H,
                                 oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16, inp.tables,
                                 inp.scales, inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha,
@@ -64,6 +71,8 @@ def to_device(inp: HostInputs, device="cuda"):
         history=None if inp.history is None else torch.from_numpy(inp.history).to(device),
         streams=torch.from_numpy(inp.streams.view(np.int16)).to(device),
         alpha=torch.from_numpy(inp.alpha).to(device),
+        positions=None if inp.positions is None else torch.from_numpy(inp.positions).to(device),
+        dead=None if inp.dead is None else torch.from_numpy(inp.dead).to(device),
     )
     if cfg.dtype == W.FP8:
         tabs = [torch.from_numpy(t).to(device) for t in inp.tables]
@@ -80,12 +89,13 @@ def gpu_path(cfg: W.EngramConfig, dev: dict, aux: bool = True, in_place: bool = 
     import torch
     import hashed_gram_memory_gb300 as eg
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    eids = eg.engram_compress(dev["ids"], dev["tid2eid"], cfg.n_eids, status=status)
+    eids = eg.engram_compress(dev["ids"], dev["tid2eid"], cfg.n_eids, status=status,
+                              dead=dev.get("dead"))
     hist_out = None
     if dev["history"] is not None:
         hist_out = torch.empty_like(dev["history"])
     rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=dev["history"], history_out=hist_out,
-                          status=status)
+                          status=status, positions=dev.get("positions"))
     gate = torch.full((cfg.T,), float("nan"), device="cuda") if aux else None
     mem = torch.full((cfg.T, cfg.D), float("nan"), device="cuda") if aux else None
     x = dev["streams"]

@@ -32,7 +32,8 @@ def declared():
 
 def test_header_declares_the_boundary():
     names = declared()
-    for n in ("engram_compress", "engram_hash", "engram_lookup_fused", "engram_read_status",
+    for n in ("engram_compress", "engram_compress_masked", "engram_hash", "engram_hash_packed",
+              "engram_lookup_fused", "engram_read_status",
               "engram_status_string", "engram_last_error", "engram_abi_version"):
         assert n in names
 
@@ -55,7 +56,7 @@ def test_library_exports_every_declared_symbol(eg):
 
 
 def test_abi_version_and_strings(eg):
-    assert eg.engram_abi_version() == 1
+    assert eg.engram_abi_version() == 2
     for code in range(6):
         assert eg.engram_status_string(code).startswith("ENGRAM")
     assert "unknown" in eg.engram_status_string(99)

@@ -172,3 +172,43 @@ def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg):
         eg.engram_debug_withhold_copies(0)
         eg.engram_set_wait_limit_ns(prev_l)
         eg.engram_set_lookup_kernel(prev_k)
+
+
+@pytest.mark.parametrize("pos", [0, 1, 2, 3, 40])
+def test_decode_positions_and_dead_history_match_oracle(eg, pos):
+    """Decode steps of packed requests: the start position bounds how far back the
+    history is read, a dead history entry blocks the lookback, dead tokens pass
+    through; the history updated in place carries the dead markers."""
+    import torch
+    g = np.random.default_rng(30 + pos)
+    B = 7
+    hist = g.integers(1, 100_000, size=(B, 3)).astype(np.int32)
+    hist[1, 1] = oracle.DEAD
+    hist[4, 2] = oracle.DEAD
+    eids = g.integers(1, 100_000, size=(B, 1)).astype(np.int32)
+    eids[5, 0] = oracle.DEAD
+    positions = np.full((B, 1), pos, np.int32)
+    positions[6, 0] = 1
+    rows = (10007, 10009, 10037)
+    ref, href, flags = oracle.hash_ids(eids, 4, rows, history=hist, want_history=True,
+                                       positions=positions)
+    assert flags == 0
+    h = _t(hist)
+    got = eg.engram_hash(_t(eids), 4, rows, history=h, history_out=h, positions=_t(positions))
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert np.array_equal(h.cpu().numpy(), href)
+    torch.cuda.synchronize()
+
+
+def test_masked_compress_matches_oracle(eg):
+    g = np.random.default_rng(5)
+    m = g.integers(1, 50, size=64).astype(np.int32)
+    ids = g.integers(-3, 70, size=200).astype(np.int32)
+    dead = (g.random(200) < 0.3).astype(np.uint8)
+    ref, rflags = oracle.compress_masked(ids, m, 49, dead, fill=-7)
+    import torch
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((200,), -7, dtype=torch.int32, device="cuda")
+    eg.engram_compress(_t(ids), _t(m), 49, eids_out=out, status=st, dead=_t(dead))
+    assert eg.engram_read_status(st)[1] == rflags
+    assert np.array_equal(out.cpu().numpy(), ref)

@@ -30,10 +30,10 @@ def run_full(eg, cfg, device_inputs):
     import torch
     d = device_inputs
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    eids = eg.engram_compress(d["ids"], d["tid2eid"], cfg.n_eids, status=st)
+    eids = eg.engram_compress(d["ids"], d["tid2eid"], cfg.n_eids, status=st, dead=d["dead"])
     hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
     rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=d["history"], history_out=hist_out,
-                          status=st)
+                          status=st, positions=d["positions"])
     out = torch.empty_like(d["streams"])
     eg.engram_lookup_fused(rows, cfg.H, d["tables"], d["streams"], d["alpha"], cfg.eps,
                            streams_out=out, status=st)
@@ -46,7 +46,10 @@ def device_inputs(eg, cfg):
     tabs, scales = W.tables_device(cfg, "cuda")
     dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
     hist = W.history(cfg)
+    pos, dead = W.packed_layout(cfg) if cfg.packed else (None, None)
     return dict(ids=torch.from_numpy(W.token_ids(cfg)).cuda(),
+                positions=None if pos is None else torch.from_numpy(pos).cuda(),
+                dead=None if dead is None else torch.from_numpy(dead).cuda(),
                 tid2eid=torch.from_numpy(W.tid2eid(cfg)).cuda(),
                 history=None if hist is None else torch.from_numpy(hist).cuda(),
                 streams=W.streams_device(cfg, "cuda"),
@@ -54,7 +57,7 @@ def device_inputs(eg, cfg):
                 tables=eg.Tables(dt, tabs, scales))
 
 
-@pytest.mark.parametrize("ci", [1, 2, 3, 4])
+@pytest.mark.parametrize("ci", [1, 2, 3, 4, 5])
 def test_full_size_sampled(eg, ci):
     import torch
     cfg = W.CONFIGS[ci]
@@ -68,9 +71,15 @@ def test_full_size_sampled(eg, ci):
 
     # every index, bit-exact
     ids_h = d["ids"].cpu().numpy()
-    e_ref, f1 = oracle.compress(ids_h, d["tid2eid"].cpu().numpy(), cfg.n_eids)
+    if d["dead"] is not None:
+        e_ref, f1 = oracle.compress_masked(ids_h, d["tid2eid"].cpu().numpy(), cfg.n_eids,
+                                           d["dead"].cpu().numpy())
+    else:
+        e_ref, f1 = oracle.compress(ids_h, d["tid2eid"].cpu().numpy(), cfg.n_eids)
     hist_h = None if d["history"] is None else d["history"].cpu().numpy()
-    r_ref, h_ref, f2 = oracle.hash_ids(e_ref, cfg.H, cfg.rows, history=hist_h, want_history=True)
+    pos_h = None if d["positions"] is None else d["positions"].cpu().numpy()
+    r_ref, h_ref, f2 = oracle.hash_ids(e_ref, cfg.H, cfg.rows, history=hist_h, want_history=True,
+                                       positions=pos_h)
     assert f1 == f2 == 0
     assert np.array_equal(eids.cpu().numpy(), e_ref)
     assert np.array_equal(rows.cpu().numpy(), r_ref)
@@ -85,8 +94,9 @@ def test_full_size_sampled(eg, ci):
     tabs, scs, remap = [], [], np.empty_like(rr)
     for n in range(3):
         cols = slice(n * cfg.H, (n + 1) * cfg.H)
-        uniq, inv = np.unique(rr[:, cols], return_inverse=True)
-        remap[:, cols] = inv.reshape(rr[:, cols].shape)
+        live = rr[:, cols] != oracle.DEAD
+        uniq, inv = np.unique(np.where(live, rr[:, cols], 0), return_inverse=True)
+        remap[:, cols] = np.where(live, inv.reshape(rr[:, cols].shape), oracle.DEAD)
         idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
         t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
         tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))

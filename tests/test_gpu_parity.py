@@ -26,6 +26,11 @@ SMALL = {
     "d16_h32_bf16": C[4].scaled(B=2, S=41, D=16, H=32, rows=(1, 2, 3), bf16_std=1.0),
     "d4096_h32": C[3].scaled(B=1, S=19, H=32, rows=(50, 60, 70)),
     "d2560_decode": C[2].scaled(B=37, D=2560, rows=(97, 89, 83)),
+    "packed_mm_fp8": C[5].scaled(B=2, S=611, rows=(4099, 5003, 6007), mean_sample_len=90,
+                                 image_span=24),
+    "packed_mm_loud_h4": C[5].scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
+                                     scale_hi=1.0, mean_sample_len=40, image_span=8,
+                                     image_frac=0.4),
 }
 
 

@@ -247,7 +247,7 @@ def test_brute_force_python_ints_tiny():
 
 
 def test_hash_flags_negative_eids_and_skips_token():
-    eids = np.array([[3, 4, -1, 5, 6, 7, 8]], np.int32)
+    eids = np.array([[3, 4, -2, 5, 6, 7, 8]], np.int32)   # -1 is the dead marker, -2 invalid
     ids, flags = oracle.hash_ids(eids, 1, [101, 103, 107], fill=-7)
     assert flags == oracle.BAD_EID
     # windows s-3..s containing position 2: s = 2..5 are skipped
@@ -491,3 +491,94 @@ def test_lookup_in_place_equals_out_of_place():
     oracle.lib().orc_lookup(ids.ctypes.data, ids.shape[0], 3, oracle.BF16, x.shape[-1], tp, sp, r,
                             xx.ctypes.data, alpha.ctypes.data, 1e-6, xx.ctypes.data, None, None)
     assert (xx == y).all()
+
+
+# ----------------------------------------------------------------- dead positions, packed samples
+
+def test_compress_masked_marks_dead_whatever_the_token():
+    m = np.array([0, 5, 9, 2], np.int32)
+    ids = np.array([1, -5, 2, 7, 3], np.int32)
+    dead = np.array([0, 1, 0, 1, 0], np.uint8)
+    out, flags = oracle.compress_masked(ids, m, 10, dead)
+    assert flags == 0 and out.tolist() == [5, oracle.DEAD, 9, oracle.DEAD, 2]
+
+
+def test_dead_token_blocks_lookback_like_a_sequence_start():
+    """A blocked lookback and the pad before position 0 agree (VeOmni PR page,
+    pack_ngram_inputs commit): the tokens after a dead one hash exactly like a
+    fresh sequence, the tokens before it are untouched, the dead token itself has
+    only dead rows."""
+    g = np.random.default_rng(21)
+    e = g.integers(1, 100_000, size=(1, 14)).astype(np.int32)
+    p = 5
+    ed = e.copy()
+    ed[0, p] = oracle.DEAD
+    plain, _ = oracle.hash_ids(e, 3, BIG_ROWS)
+    got, flags = oracle.hash_ids(ed, 3, BIG_ROWS)
+    assert flags == 0
+    assert (got[0, :p] == plain[0, :p]).all()
+    assert (got[0, p] == oracle.DEAD).all()
+    fresh, _ = oracle.hash_ids(e[:, p + 1:], 3, BIG_ROWS)
+    assert (got[0, p + 1:] == fresh[0]).all()
+
+
+def test_packed_samples_hash_like_separate_sequences():
+    """Positions restarting at 0 per packed sample keep every n-gram inside its
+    sample (VeOmni PR page, review of pack_ngram_inputs)."""
+    g = np.random.default_rng(22)
+    lens = [5, 1, 9, 2]
+    samples = [g.integers(1, 100_000, size=n).astype(np.int32) for n in lens]
+    packed = np.concatenate(samples)[None, :]
+    positions = np.concatenate([np.arange(n) for n in lens]).astype(np.int32)[None, :]
+    got, flags = oracle.hash_ids(packed, 2, BIG_ROWS, positions=positions)
+    assert flags == 0
+    parts = [oracle.hash_ids(smp[None, :], 2, BIG_ROWS)[0][0] for smp in samples]
+    assert (got[0] == np.concatenate(parts)).all()
+    # positions equal to the index reproduce the plain hash
+    same, _ = oracle.hash_ids(packed, 2, BIG_ROWS, positions=np.arange(17, dtype=np.int32)[None, :])
+    plain, _ = oracle.hash_ids(packed, 2, BIG_ROWS)
+    assert (same == plain).all()
+
+
+@pytest.mark.parametrize("pos", [0, 1, 2, 3, 50])
+def test_decode_start_position_bounds_the_history(pos):
+    """The history sets how far back the walk can read, the start position whether
+    it reached the true start (VeOmni PR page, decode cache commit): a step at
+    position p hashes like the last token of the p+1-token sequence whose first
+    ids are the history tail."""
+    hist = np.array([[11, 22, 33]], np.int32)
+    tok = np.array([[44]], np.int32)
+    got, _ = oracle.hash_ids(tok, 2, BIG_ROWS, history=hist, positions=np.array([[pos]], np.int32))
+    seq = np.concatenate([hist[0, 3 - min(pos, 3):], tok[0]])[None, :]
+    ref, _ = oracle.hash_ids(seq, 2, BIG_ROWS)
+    assert (got[0, 0] == ref[0, -1]).all()
+
+
+def test_dead_history_entry_blocks_and_is_carried():
+    hist = np.array([[11, oracle.DEAD, 33]], np.int32)
+    tok = np.array([[44, 55]], np.int32)
+    got, hout, _ = oracle.hash_ids(tok, 2, BIG_ROWS, history=hist, want_history=True)
+    ref, _ = oracle.hash_ids(np.array([[33, 44, 55]], np.int32), 2, BIG_ROWS)
+    assert (got[0] == ref[0, 1:]).all()
+    assert hout.tolist() == [[33, 44, 55]]
+    _, hout2, _ = oracle.hash_ids(np.array([[oracle.DEAD]], np.int32), 2, BIG_ROWS, history=hist,
+                                  want_history=True)
+    assert hout2.tolist() == [[oracle.DEAD, 33, oracle.DEAD]]
+
+
+def test_dead_tokens_pass_through_with_zero_gate():
+    """A dead token's gate is zeroed (vLLM page, DeepseekV4Model.forward): its
+    streams come out bit for bit, g = 0, m = 0; a token with some dead and some
+    live row ids is a bad row."""
+    tabs, scales, ids, x, alpha = _random_case(oracle.FP8, seed=11)
+    ids = ids.copy()
+    ids[3] = oracle.DEAD
+    ids[6, 2] = oracle.DEAD
+    y, gate, m, flags = oracle.lookup(ids, 3, oracle.FP8, tabs, scales, x, alpha, 1e-6, aux=True,
+                                      fill=0x1234)
+    assert flags == oracle.BAD_ROW
+    assert (y[3] == x[3]).all() and gate[3] == 0 and (m[3] == 0).all()
+    assert (y[6] == 0x1234).all()
+    live = [t for t in range(ids.shape[0]) if t not in (3, 6)]
+    y2, _ = oracle.lookup(ids[live], 3, oracle.FP8, tabs, scales, x[live], alpha, 1e-6)
+    assert (y[live] == y2).all()

@@ -27,7 +27,7 @@ import dataclasses
 import numpy as np
 
 # Input kinds: one independent PCG64 stream per kind.
-_K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS = range(8)
+_K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS, _K_PACK = range(9)
 
 FP8 = "fp8_e4m3fn"
 BF16 = "bf16"
@@ -53,6 +53,10 @@ class EngramConfig:
     id_range: int = 0      # uniform ids in [0, id_range); 0 means [0, vocab)
     repeat_frac: float = 0.0   # fraction of positions that copy an earlier 4-token span
     decode: bool = False   # one new token per slot with a 3-id history
+    packed: bool = False   # samples packed into each row; positions restart per sample
+    mean_sample_len: int = 0
+    image_span: int = 0    # length of one image span (dead positions)
+    image_frac: float = 0.0  # target fraction of positions inside image spans
     bf16_std: float = 0.02
     scale_lo: float = 1e-3
     scale_hi: float = 1e-2
@@ -100,6 +104,12 @@ CONFIGS = [
     # 4: BF16 tables, uniform (cache-hostile) ids
     EngramConfig(name="bf16_tables", seed=4, B=4, S=8192, vocab=129_280, n_eids=100_000, H=4,
                  D=4096, rows=(5_040_000,) * 3, dtype=BF16, ids="uniform"),
+    # 5: packed multimodal prefill: samples of ~1024 tokens packed into each row
+    #    (positions restart per sample), a quarter of the positions in 256-token
+    #    image spans (dead); otherwise the full-size prefill
+    EngramConfig(name="packed_mm_fp8", seed=5, B=8, S=8192, vocab=129_280, n_eids=100_000,
+                 H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8, ids="zipf", packed=True,
+                 mean_sample_len=1024, image_span=256, image_frac=0.25),
 ]
 
 
@@ -151,6 +161,33 @@ def token_ids(cfg: EngramConfig, rank: int = 0) -> np.ndarray:
     if cfg.repeat_frac > 0:
         plant_repeats(ids, cfg.repeat_frac, rng(cfg, _K_SPANS, rank))
     return np.ascontiguousarray(ids)
+
+
+def packed_layout(cfg: EngramConfig, rank: int = 0):
+    """(positions [B, S] int32, dead [B, S] uint8) of a packed batch: every row is
+    cut into samples of U[L/2, 3L/2] tokens (L = mean_sample_len, the last one cut
+    at the row's end), positions count from 0 in each sample, and a sample holds
+    one image span of image_span dead positions at a uniform offset with
+    probability image_frac * len / image_span (capped at 1)."""
+    B, S = cfg.B, cfg.S
+    pos = np.zeros((B, S), np.int32)
+    dead = np.zeros((B, S), np.uint8)
+    if not cfg.packed:
+        pos[:] = np.arange(S, dtype=np.int32)[None, :]
+        return pos, dead
+    g = rng(cfg, _K_PACK, rank)
+    L = max(1, cfg.mean_sample_len)
+    for b in range(B):
+        s0 = 0
+        while s0 < S:
+            n = int(min(S - s0, g.integers(max(1, L // 2), L + L // 2 + 1)))
+            pos[b, s0:s0 + n] = np.arange(n, dtype=np.int32)
+            span = cfg.image_span
+            if span and n > span and g.random() < min(1.0, cfg.image_frac * n / span):
+                off = int(g.integers(0, n - span + 1))
+                dead[b, s0 + off:s0 + off + span] = 1
+            s0 += n
+    return pos, dead
 
 
 def tid2eid(cfg: EngramConfig) -> np.ndarray:
