@@ -174,7 +174,7 @@ class ClockSampler:
 def device_inputs(eg, cfg, rank, device):
     import torch
     tabs, scales = W.tables_device(cfg, device)
-    dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
+    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16}[cfg.dtype]
     hist = W.history(cfg, rank)
     pos, dead = W.packed_layout(cfg, rank) if cfg.packed else (None, None)
     return dict(
@@ -418,11 +418,16 @@ def oracle_sample(cfg, d, n_tokens):
         remap[:, cols] = np.where(live, inv.reshape(r[:, cols].shape), oracle.DEAD)
         idx = torch.from_numpy(uniq.astype(np.int64)).to(d["tables"].tables[k].device)
         t = d["tables"].tables[k].index_select(0, idx).cpu().numpy()
-        host_tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))
+        host_tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
         host_scales.append(d["tables"].scales[k].index_select(0, idx).cpu().numpy()
-                           if cfg.dtype == W.FP8 else None)
+                           if cfg.dtype != W.BF16 else None)
     return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=x, tables=host_tabs, scales=host_scales,
                 remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n, dead=dead, positions=pos)
+
+
+def oracle_dtype(cfg):
+    import oracle
+    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.BF16: oracle.BF16}[cfg.dtype]
 
 
 def time_oracle(cfg, s, repeats=1):
@@ -435,8 +440,8 @@ def time_oracle(cfg, s, repeats=1):
         else:
             e, _ = oracle.compress(s["ids"], s["tid2eid"], cfg.n_eids)
         oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"], positions=s.get("positions"))
-        oracle.lookup(s["remap"], cfg.H, oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16,
-                      s["tables"], s["scales"], s["x"], s["alpha"], cfg.eps)
+        oracle.lookup(s["remap"], cfg.H, oracle_dtype(cfg), s["tables"], s["scales"], s["x"],
+                      s["alpha"], cfg.eps)
     return (time.perf_counter() - t0) / repeats
 
 
@@ -477,6 +482,10 @@ def reference_sample(cfg, n):
         if cfg.dtype == W.FP8:
             tabs.append(W._to_e4m3_bytes(x))
             scs.append(g.uniform(cfg.scale_lo, cfg.scale_hi, len(uniq)).astype(np.float32))
+        elif cfg.dtype == W.FP8_E8M0:
+            tabs.append(W._to_e4m3_bytes(x))
+            scs.append(g.integers(cfg.e8m0_lo, cfg.e8m0_hi + 1, size=(len(uniq), cfg.D // 32))
+                       .astype(np.uint8))
         else:
             tabs.append(W._to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scs.append(None)

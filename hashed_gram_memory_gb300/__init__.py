@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libengram.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_TIMEOUT = range(6)
 FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
-TABLE_FP8_E4M3FN, TABLE_BF16 = 0, 1
+TABLE_FP8_E4M3FN, TABLE_BF16, TABLE_FP8_E8M0 = 0, 1, 2
 EID_DEAD = ROW_DEAD = -1
 LOOKUP_AUTO, LOOKUP_GATHER, LOOKUP_BULK = 0, 1, 2
 MAX_HEADS, MAX_D = 32, 4096
@@ -117,7 +117,9 @@ def _need(t, dtypes, name, contiguous=True):
 
 @dataclasses.dataclass
 class Tables:
-    """The three device tables (orders 2, 3, 4) and, for FP8, their fp32 row scales."""
+    """The three device tables (orders 2, 3, 4) and their scales: fp32 [rows] for
+    TABLE_FP8_E4M3FN, uint8 e8m0 exponents [rows, D/32] for TABLE_FP8_E8M0, none
+    for TABLE_BF16."""
 
     dtype: int
     tables: list

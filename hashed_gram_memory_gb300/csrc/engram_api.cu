@@ -208,14 +208,17 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
   if (!tables_host) return fail(ENGRAM_ERR_INVALID_ARG, "%s: tables is NULL", fn);
   const engram_tables &tb = *tables_host;
-  if (tb.dtype != ENGRAM_TABLE_FP8_E4M3FN && tb.dtype != ENGRAM_TABLE_BF16)
+  if (tb.dtype != ENGRAM_TABLE_FP8_E4M3FN && tb.dtype != ENGRAM_TABLE_BF16 &&
+      tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: unknown table dtype %d", fn, tb.dtype);
   if (tb.D < 16 || tb.D % 16 != 0)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: D = %d must be a positive multiple of 16", fn, tb.D);
+  if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && tb.D % 32 != 0)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: E8M0 (1, 32) blocks need D %% 32 == 0", fn);
   if (tb.D > ENGRAM_MAX_D)
     return fail(ENGRAM_ERR_UNSUPPORTED, "%s: D = %d exceeds %d", fn, tb.D, ENGRAM_MAX_D);
   const int D = tb.D;
-  const size_t elt = tb.dtype == ENGRAM_TABLE_FP8_E4M3FN ? 1 : 2;
+  const size_t elt = tb.dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
   for (int n = 0; n < 3; ++n) {
     if (tb.rows[n] < 1 || tb.rows[n] > INT32_MAX)
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: rows[%d] must be in [1, 2^31-1]", fn, n);
@@ -223,6 +226,8 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: table[%d] NULL or not 16-byte aligned", fn, n);
     if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN && (!tb.scale[n] || !aligned(tb.scale[n], 4)))
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: scale[%d] NULL or not 4-byte aligned", fn, n);
+    if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && (!tb.scale[n] || !aligned(tb.scale[n], 16)))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: scale[%d] NULL or not 16-byte aligned", fn, n);
   }
   if (!alpha || !aligned(alpha, 4))
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: alpha NULL or not 4-byte aligned", fn);

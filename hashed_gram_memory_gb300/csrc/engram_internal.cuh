@@ -43,7 +43,7 @@ struct HashParams {
 struct LookupParams {
   const int32_t *row_ids;
   const uint8_t *table[3];
-  const float *scale[3];
+  const void *scale[3];  // float [rows] (FP8), uint8 [rows, D/32] (FP8 + E8M0 blocks)
   int64_t rows[3];
   const uint16_t *x;  // streams in  [T, 4, D]
   uint16_t *y;        // streams out [T, 4, D]

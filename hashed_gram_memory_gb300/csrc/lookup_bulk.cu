@@ -4,7 +4,9 @@
 // One token per CTA of D/16 threads (16 columns each).  Thread 0 issues all 3H
 // row copies of the token at once (one contiguous D*elt-byte run per row, one
 // cp.async.bulk each) completing on a single mbarrier that expects their total
-// byte count, while the other threads fetch the row scales into shared memory
+// byte count (with the row's 32-column block exponents when the table has
+// them, one more bulk copy per row), while the other threads fetch the row
+// scales into shared memory
 // and, for large tokens, the four 32-byte stream slices into registers with
 // evict-first loads.  After the wait every thread reads its columns of the rows
 // from shared memory, accumulates the dequantised rows in fp32, the gate sums
@@ -85,14 +87,17 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns) {
 template <int DT, bool AUX, bool EARLY>
 __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
     lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
-  constexpr bool kFp8 = DT == ENGRAM_TABLE_FP8_E4M3FN;
+  constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;                // FP8 bytes
+  constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
   constexpr int kElt = kFp8 ? 1 : 2;
   extern __shared__ __align__(128) uint8_t sm[];
 
   const int H = p.H, R = 3 * H, D = p.D;
   const uint32_t row_bytes = (uint32_t)D * kElt;
+  const uint32_t exp_bytes = kE8 ? (uint32_t)D / 32 : 0;         // a row's block exponents
   uint8_t *s_rows = sm;                                          // [R][row_bytes]
-  uint64_t *bar = reinterpret_cast<uint64_t *>(s_rows + (size_t)R * row_bytes);
+  uint8_t *s_exps = s_rows + (size_t)R * row_bytes;              // [R][exp_bytes]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(s_exps + (size_t)R * exp_bytes);
   float *s_scale = reinterpret_cast<float *>(bar + 1);           // [R]
   float *s_red = s_scale + kMaxRows;                             // [8][3]
 
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
 
   // Thread 0: every row copy of the token on the one barrier.
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)R * row_bytes);
+    mbar_arrive_expect_tx(bar, (uint32_t)R * (row_bytes + exp_bytes));
     bool withhold = p.withhold != 0;
     for (int r = 0; r < R; ++r) {
       const int ni = (r >= H) + (r >= 2 * H);
@@ -141,13 +146,17 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
       }
       bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + (int64_t)ids[r] * row_bytes, row_bytes,
                bar);
+      if (kE8)
+        bulk_g2s(s_exps + (size_t)r * exp_bytes,
+                 static_cast<const uint8_t *>(p.scale[ni]) + (int64_t)ids[r] * exp_bytes, exp_bytes,
+                 bar);
     }
   }
   // Meanwhile: the row scales into shared memory, the stream slices into registers.
-  if (kFp8) {
+  if (kFp8 && !kE8) {
     for (int r = tid; r < R; r += blockDim.x) {
       const int ni = (r >= H) + (r >= 2 * H);
-      s_scale[r] = __ldg(p.scale[ni] + ids[r]);
+      s_scale[r] = __ldg(static_cast<const float *>(p.scale[ni]) + ids[r]);
     }
   }
   uint4 xs[4][2];
@@ -179,7 +188,8 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   for (int r = 0; r < R; ++r) {
     const uint8_t *row = src + (size_t)r * row_bytes;
     if (kFp8) {
-      acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), s_scale[r]);
+      const float scale = kE8 ? e8m0_to_float(s_exps[(size_t)r * exp_bytes + (col0 >> 5)]) : s_scale[r];
+      acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), scale);
     } else {
       acc_bf16(acc, *reinterpret_cast<const uint4 *>(row));
       acc_bf16(acc + 8, *reinterpret_cast<const uint4 *>(row + 16));
@@ -259,8 +269,9 @@ cudaError_t launch_bulk_dt(const LookupParams &p, size_t smem, bool aux, bool ea
 }  // namespace
 
 size_t bulk_smem_bytes(int D, int dtype, int H) {
-  const size_t elt = dtype == ENGRAM_TABLE_FP8_E4M3FN ? 1 : 2;
-  return (size_t)3 * H * D * elt + 8 + kMaxRows * 4 + 24 * 4;
+  const size_t elt = dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
+  const size_t exps = dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 ? (size_t)3 * H * (D / 32) : 0;
+  return (size_t)3 * H * D * elt + exps + 8 + kMaxRows * 4 + 24 * 4;
 }
 
 // D a multiple of 512 (whole warps of 16-column threads, at most 256 threads) and
@@ -279,6 +290,8 @@ cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t st
   const bool early = smem > 56 * 1024;
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
     return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+    return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32>(p, smem, aux, early, stream);
   return launch_bulk_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 

@@ -9,6 +9,11 @@
 
 namespace engram {
 
+// OCP E8M0 exponent -> fp32: 2^(e-127) (e = 0 is the fp32 subnormal 2^-127), 0xFF NaN.
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
+  return __uint_as_float(e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -29,7 +29,8 @@ __device__ __forceinline__ uint4 ld_row16(const uint8_t *ptr) {
 
 template <int DT, bool AUX>
 __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ LookupParams p) {
-  constexpr bool kFp8 = DT == ENGRAM_TABLE_FP8_E4M3FN;
+  constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;           // FP8 bytes (row or block scales)
+  constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
   constexpr int kElt = kFp8 ? 1 : 2;         // bytes per table element
   constexpr int kVecPerRow = kFp8 ? 1 : 2;   // 16-byte loads per row per thread
   constexpr int kBatch = kFp8 ? 8 : 4;       // rows in flight per thread
@@ -101,7 +102,11 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
           const uint8_t *base = p.table[ni] + (row * p.D + col0) * kElt;
           v[k][0] = ld_row16(base);
           if (!kFp8) v[k][1] = ld_row16(base + 16);
-          if (kFp8) sc[k] = __ldg(p.scale[ni] + row);
+          if (kE8)
+            sc[k] = e8m0_to_float(__ldg(static_cast<const uint8_t *>(p.scale[ni]) +
+                                        row * (p.D >> 5) + (col0 >> 5)));
+          else if (kFp8)
+            sc[k] = __ldg(static_cast<const float *>(p.scale[ni]) + row);
         }
       }
 #pragma unroll
@@ -214,6 +219,9 @@ cudaError_t launch_lookup(const LookupParams &p_in, int dtype, cudaStream_t stre
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
     return aux ? launch_t<ENGRAM_TABLE_FP8_E4M3FN, true>(p, threads, smem, stream)
                : launch_t<ENGRAM_TABLE_FP8_E4M3FN, false>(p, threads, smem, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+    return aux ? launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, true>(p, threads, smem, stream)
+               : launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, false>(p, threads, smem, stream);
   return aux ? launch_t<ENGRAM_TABLE_BF16, true>(p, threads, smem, stream)
              : launch_t<ENGRAM_TABLE_BF16, false>(p, threads, smem, stream);
 }

@@ -75,6 +75,7 @@ typedef int32_t engram_status;
 
 #define ENGRAM_TABLE_FP8_E4M3FN 0
 #define ENGRAM_TABLE_BF16 1
+#define ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 2
 
 /*
  * Dead positions (image spans: vLLM page, DeepseekV4Model.forward, they break
@@ -90,19 +91,25 @@ typedef int32_t engram_status;
 
 /*
  * The three n-gram tables (index 0, 1, 2 = orders 2, 3, 4), row-major
- * [rows[n], D], each 16-byte aligned.  FP8: one byte per element (OCP E4M3,
- * "fn": bias 7, max 448, no infinities) and scale[n] = fp32 [rows[n]], the
- * row's dequantisation factor (VeOmni PR page: FP8 tables with row-wise
- * dequantisation on lookup).  BF16: two bytes per element, scale[n] ignored.
+ * [rows[n], D], each 16-byte aligned, in one of three formats:
+ *  - ENGRAM_TABLE_FP8_E4M3FN: one byte per element (OCP E4M3, "fn": bias 7, max
+ *    448, no infinities); scale[n] = float [rows[n]], the row's dequantisation
+ *    factor (VeOmni PR page: FP8 tables with row-wise dequantisation on lookup).
+ *  - ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32: the same bytes; scale[n] = uint8
+ *    [rows[n], D/32], one OCP E8M0 exponent per row per 32 columns (value
+ *    2^(e-127), 0xFF NaN), 16-byte aligned; D % 32 == 0 (VeOmni PR page: the
+ *    release blocks its tables (1, 32)).  The products are exact powers of two
+ *    times the FP8 value, within the fp32 range.
+ *  - ENGRAM_TABLE_BF16: two bytes per element; scale[n] ignored.
  * 1 <= rows[n] <= 2^31 - 1.  The struct itself is read on the host during the
  * call only.
  */
 typedef struct engram_tables {
-  int32_t dtype; /* ENGRAM_TABLE_FP8_E4M3FN or ENGRAM_TABLE_BF16 */
-  int32_t D;     /* row width, multiple of 16, 16..ENGRAM_MAX_D */
+  int32_t dtype; /* ENGRAM_TABLE_* */
+  int32_t D;     /* row width, multiple of 16 (32 for E8M0 blocks), 16..ENGRAM_MAX_D */
   int64_t rows[3];
   const void *table[3];
-  const float *scale[3];
+  const void *scale[3];
 } engram_tables;
 
 /*

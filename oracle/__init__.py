@@ -16,6 +16,7 @@ from . import build as _build
 
 FP8 = 0
 BF16 = 1
+FP8_E8M0 = 2
 DEAD = -1
 BAD_TOKEN, BAD_EID, BAD_ROW, BAD_ARG = 1, 2, 4, 16
 
@@ -38,6 +39,8 @@ def lib():
         L.orc_e4m3fn_decode.argtypes = [C.c_uint8]
         L.orc_bf16_decode.restype = C.c_double
         L.orc_bf16_decode.argtypes = [C.c_uint16]
+        L.orc_e8m0_decode.restype = C.c_double
+        L.orc_e8m0_decode.argtypes = [C.c_uint8]
         L.orc_bf16_round.restype = C.c_uint16
         L.orc_bf16_round.argtypes = [C.c_double]
         L.orc_compress.restype = C.c_int
@@ -96,6 +99,10 @@ def bf16_decode(bits: int) -> float:
     return float(lib().orc_bf16_decode(bits))
 
 
+def e8m0_decode(e: int) -> float:
+    return float(lib().orc_e8m0_decode(e))
+
+
 def bf16_round(y: float) -> int:
     return int(lib().orc_bf16_round(y))
 
@@ -149,8 +156,9 @@ def lookup(row_ids, n_heads: int, dtype: int, tables, scales, streams, alpha, ep
     D = x.shape[-1]
     T = x.size // (4 * D)
     assert ids.size == T * 3 * n_heads
-    tabs = [_c(t, np.uint8 if dtype == FP8 else np.uint16) for t in tables]
-    scs = [(_c(s, np.float32) if s is not None else None) for s in scales] if scales else [None] * 3
+    tabs = [_c(t, np.uint16 if dtype == BF16 else np.uint8) for t in tables]
+    sdt = np.uint8 if dtype == FP8_E8M0 else np.float32
+    scs = [(_c(s, sdt) if s is not None else None) for s in scales] if scales else [None] * 3
     if rows is None:
         rows = [t.shape[0] for t in tabs]
     a = _c(alpha, np.float32)

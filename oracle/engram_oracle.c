@@ -69,6 +69,16 @@ double orc_e4m3fn_decode(uint8_t byte) {
   return s ? -v : v;
 }
 
+/*
+ * OCP Microscaling E8M0 scale (the pages' e8m0 block exponents, VeOmni PR page,
+ * checkpoint commits): an unsigned 8-bit exponent with bias 127 and no
+ * mantissa, 2^(e-127); 0xFF is NaN.
+ */
+double orc_e8m0_decode(uint8_t e) {
+  if (e == 0xFF) return NAN;
+  return ldexp(1.0, (int)e - 127);
+}
+
 /* bfloat16 is the upper half of an IEEE binary32: widening is exact. */
 double orc_bf16_decode(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -263,7 +273,9 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
  * The fused lookup for n_tokens tokens, one at a time, in fp64:
  *  1. gather + dequantise the 3H rows of the token: FP8 byte decoded exactly,
  *     times the row's fp32 scale (VeOmni PR page: FP8 tables with row-wise
- *     dequantisation on lookup), or the BF16 value widened exactly;
+ *     dequantisation on lookup), or times the e8m0 exponent of its row's
+ *     32-column block (the release's (1, 32) blocking), or the BF16 value
+ *     widened exactly;
  *  2. m = (sum of the 3H rows) / (3H)  (workload spec: the mean of the rows);
  *  3. with a = stream 0 of the token:
  *     g = sigmoid( sum(a*m) / (sqrt(mean(a^2)+eps) * sqrt(mean(m^2)+eps) * sqrt(D)) ),
@@ -278,11 +290,12 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
  * [n_tokens, D] are optional.
  */
 int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
-               int32_t D, const void *const tables[3], const float *const scales[3],
+               int32_t D, const void *const tables[3], const void *const scales[3],
                const int64_t rows[3], const uint16_t *streams_in, const float *alpha,
                double eps, uint16_t *streams_out, double *gate_out, double *mem_out) {
   if (n_tokens < 0 || n_heads < 1 || D < 1) return ORC_BAD_ARG;
-  if (dtype != ORC_FP8_E4M3FN && dtype != ORC_BF16) return ORC_BAD_ARG;
+  if (dtype != ORC_FP8_E4M3FN && dtype != ORC_BF16 && dtype != ORC_FP8_E8M0_B32) return ORC_BAD_ARG;
+  if (dtype == ORC_FP8_E8M0_B32 && D % 32) return ORC_BAD_ARG;
   const int R = 3 * n_heads;
   int flags = 0;
 #pragma omp parallel for schedule(dynamic, 16) reduction(| : flags)
@@ -319,7 +332,13 @@ int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_
         double v;
         if (dtype == ORC_FP8_E4M3FN) {
           const uint8_t *tab = (const uint8_t *)tables[n];
-          v = orc_e4m3fn_decode(tab[row * D + i]) * (double)scales[n][row];
+          v = orc_e4m3fn_decode(tab[row * D + i]) * (double)((const float *)scales[n])[row];
+        } else if (dtype == ORC_FP8_E8M0_B32) {
+          /* (1, 32) blocks: one exponent per row per 32 columns (VeOmni PR page, the
+           * commit on the tables' per-row block scales) */
+          const uint8_t *tab = (const uint8_t *)tables[n];
+          const uint8_t *sc = (const uint8_t *)scales[n];
+          v = orc_e4m3fn_decode(tab[row * D + i]) * orc_e8m0_decode(sc[row * (D / 32) + i / 32]);
         } else {
           const uint16_t *tab = (const uint16_t *)tables[n];
           v = orc_bf16_decode(tab[row * D + i]);

@@ -33,6 +33,7 @@ extern "C" {
 
 #define ORC_FP8_E4M3FN 0
 #define ORC_BF16 1
+#define ORC_FP8_E8M0_B32 2 /* FP8 e4m3fn + one e8m0 exponent per row per 32 columns */
 
 /* A dead position (an image span): compresses to this marker, blocks every
  * n-gram that would span it, and its token's row ids are all ORC_DEAD. */
@@ -43,6 +44,7 @@ uint64_t orc_seed(int n, int j);
 uint64_t orc_ngram_hash(const int32_t *window, int n, int j);
 double orc_e4m3fn_decode(uint8_t byte);
 double orc_bf16_decode(uint16_t bits);
+double orc_e8m0_decode(uint8_t e);
 uint16_t orc_bf16_round(double y);
 
 int orc_compress(const int32_t *token_ids, int64_t n, const int32_t *tid2eid, int32_t vocab,
@@ -60,7 +62,7 @@ int orc_hash_packed(const int32_t *eids, int32_t B, int32_t S, const int32_t *po
                     int32_t *row_ids_out, int32_t *history_out);
 
 int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
-               int32_t D, const void *const tables[3], const float *const scales[3],
+               int32_t D, const void *const tables[3], const void *const scales[3],
                const int64_t rows[3], const uint16_t *streams_in, const float *alpha,
                double eps, uint16_t *streams_out, double *gate_out, double *mem_out);
 

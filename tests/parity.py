@@ -45,6 +45,10 @@ def host_inputs(cfg: W.EngramConfig, rank: int = 0) -> HostInputs:
                       scales, W.streams_host(cfg, rank), W.alpha(cfg), pos, dead)
 
 
+def oracle_dtype(cfg: W.EngramConfig) -> int:
+    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.BF16: oracle.BF16}[cfg.dtype]
+
+
 def oracle_path(inp: HostInputs):
     cfg = inp.cfg
     if inp.dead is not None:
@@ -53,8 +57,7 @@ def oracle_path(inp: HostInputs):
         eids, f1 = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
     rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history, want_history=True,
                                      positions=inp.positions)
-    y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H,
-                                oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16, inp.tables,
+    y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H, oracle_dtype(cfg), inp.tables,
                                 inp.scales, inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha,
                                 cfg.eps, aux=True)
     return dict(eids=eids, rows=rows, history=hist, streams=y.reshape(inp.streams.shape), gate=g,
@@ -74,10 +77,11 @@ def to_device(inp: HostInputs, device="cuda"):
         positions=None if inp.positions is None else torch.from_numpy(inp.positions).to(device),
         dead=None if inp.dead is None else torch.from_numpy(inp.dead).to(device),
     )
-    if cfg.dtype == W.FP8:
+    if cfg.dtype in (W.FP8, W.FP8_E8M0):
         tabs = [torch.from_numpy(t).to(device) for t in inp.tables]
         scs = [torch.from_numpy(s).to(device) for s in inp.scales]
-        dev["tables"] = eg.Tables(eg.TABLE_FP8_E4M3FN, tabs, scs)
+        dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_FP8_E8M0
+        dev["tables"] = eg.Tables(dt, tabs, scs)
     else:
         tabs = [torch.from_numpy(t.view(np.int16)).to(device) for t in inp.tables]
         dev["tables"] = eg.Tables(eg.TABLE_BF16, tabs, None)

@@ -44,7 +44,7 @@ def run_full(eg, cfg, device_inputs):
 def device_inputs(eg, cfg):
     import torch
     tabs, scales = W.tables_device(cfg, "cuda")
-    dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_BF16
+    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16}[cfg.dtype]
     hist = W.history(cfg)
     pos, dead = W.packed_layout(cfg) if cfg.packed else (None, None)
     return dict(ids=torch.from_numpy(W.token_ids(cfg)).cuda(),
@@ -57,7 +57,7 @@ def device_inputs(eg, cfg):
                 tables=eg.Tables(dt, tabs, scales))
 
 
-@pytest.mark.parametrize("ci", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("ci", [1, 2, 3, 4, 5, 6])
 def test_full_size_sampled(eg, ci):
     import torch
     cfg = W.CONFIGS[ci]
@@ -99,12 +99,12 @@ def test_full_size_sampled(eg, ci):
         remap[:, cols] = np.where(live, inv.reshape(rr[:, cols].shape), oracle.DEAD)
         idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
         t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
-        tabs.append(t.view(np.uint8) if cfg.dtype == W.FP8 else t.view(np.uint16))
+        tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
         scs.append(d["tables"].scales[n].index_select(0, idx).cpu().numpy()
-                   if cfg.dtype == W.FP8 else None)
+                   if cfg.dtype != W.BF16 else None)
     x = d["streams"].view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
-    y_ref, f3 = oracle.lookup(remap, cfg.H, oracle.FP8 if cfg.dtype == W.FP8 else oracle.BF16, tabs,
-                              scs, x, d["alpha"].cpu().numpy(), cfg.eps)
+    y_ref, f3 = oracle.lookup(remap, cfg.H, P.oracle_dtype(cfg), tabs, scs, x,
+                              d["alpha"].cpu().numpy(), cfg.eps)
     assert f3 == 0
     y = out.view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
     P.compare_streams(y, y_ref, x, what=f"{cfg.name} sampled streams")

@@ -28,6 +28,10 @@ SMALL = {
     "d2560_decode": C[2].scaled(B=37, D=2560, rows=(97, 89, 83)),
     "packed_mm_fp8": C[5].scaled(B=2, S=611, rows=(4099, 5003, 6007), mean_sample_len=90,
                                  image_span=24),
+    "e8m0_prefill_h8": C[6].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "e8m0_loud_h4_d1024": C[6].scaled(B=1, S=233, H=4, D=1024, rows=(1009, 1013, 1019),
+                                      e8m0_lo=124, e8m0_hi=129),
+    "e8m0_d96": C[6].scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41)),
     "packed_mm_loud_h4": C[5].scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
                                      scale_hi=1.0, mean_sample_len=40, image_span=8,
                                      image_frac=0.4),

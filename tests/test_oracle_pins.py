@@ -582,3 +582,56 @@ def test_dead_tokens_pass_through_with_zero_gate():
     live = [t for t in range(ids.shape[0]) if t not in (3, 6)]
     y2, _ = oracle.lookup(ids[live], 3, oracle.FP8, tabs, scales, x[live], alpha, 1e-6)
     assert (y[live] == y2).all()
+
+
+# ----------------------------------------------------------------- e8m0 block scales
+
+def test_e8m0_all_bytes_match_torch_cast():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    for e in range(256):
+        v = oracle.e8m0_decode(e)
+        assert (math.isnan(v) and math.isnan(ref[e])) or v == ref[e], e
+
+
+def test_e8m0_ocp_mx_values():
+    with open(os.path.join(GOLDEN, "e8m0_ocp_mx.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            b, v = line.split()
+            got = oracle.e8m0_decode(int(b, 16))
+            assert math.isnan(got) if v == "nan" else got == float(v), b
+
+
+def test_e8m0_blocks_gather_matches_torch_decode():
+    """m = mean over r of decode(row) * 2^(e - 127), each column with its own
+    32-column block's exponent, decoded by torch's casts."""
+    g = np.random.default_rng(12)
+    H, D, rows, T = 2, 96, (19, 23, 29), 11
+    tabs = [W._to_e4m3_bytes(g.standard_normal((r, D)).astype(np.float32) * 4) for r in rows]
+    scs = [g.integers(110, 140, size=(r, D // 32)).astype(np.uint8) for r in rows]
+    ids = np.stack([g.integers(0, rows[r // H], size=T) for r in range(3 * H)], 1).astype(np.int32)
+    x = W._to_bf16_bits(g.standard_normal((T, 4, D)).astype(np.float32))
+    _, _, m, flags = oracle.lookup(ids, H, oracle.FP8_E8M0, tabs, scs, x, np.ones(4, np.float32),
+                                   1e-6, aux=True)
+    assert flags == 0
+    acc = np.zeros((T, D))
+    for r in range(3 * H):
+        n = r // H
+        dec = torch.from_numpy(tabs[n]).view(torch.float8_e4m3fn).double().numpy()[ids[:, r]]
+        sc = torch.from_numpy(scs[n]).view(torch.float8_e8m0fnu).double().numpy()[ids[:, r]]
+        acc += dec * np.repeat(sc, 32, axis=1)
+    assert np.allclose(m, acc / (3 * H), rtol=1e-15, atol=0)
+
+
+def test_e8m0_uniform_blocks_equal_row_scales():
+    """Every block of a row sharing exponent e gives the per-row-scale result with
+    scale 2^(e - 127), bit for bit."""
+    tabs, _, ids, x, alpha = _random_case(oracle.FP8, seed=13, D=64)
+    g = np.random.default_rng(13)
+    e_rows = [g.integers(115, 125, size=t.shape[0]).astype(np.uint8) for t in tabs]
+    blocks = [np.repeat(e[:, None], 2, axis=1) for e in e_rows]
+    rows_scale = [np.ldexp(1.0, e.astype(np.int64) - 127).astype(np.float32) for e in e_rows]
+    y1, g1, m1, _ = oracle.lookup(ids, 3, oracle.FP8_E8M0, tabs, blocks, x, alpha, 1e-6, aux=True)
+    y2, g2, m2, _ = oracle.lookup(ids, 3, oracle.FP8, tabs, rows_scale, x, alpha, 1e-6, aux=True)
+    assert (y1 == y2).all() and (g1 == g2).all() and (m1 == m2).all()

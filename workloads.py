@@ -31,6 +31,7 @@ _K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS, _K_
 
 FP8 = "fp8_e4m3fn"
 BF16 = "bf16"
+FP8_E8M0 = "fp8_e4m3fn_e8m0_1x32"   # one e8m0 exponent per row per 32 columns
 E4M3_MAX = 448.0
 
 
@@ -60,6 +61,8 @@ class EngramConfig:
     bf16_std: float = 0.02
     scale_lo: float = 1e-3
     scale_hi: float = 1e-2
+    e8m0_lo: int = 117     # block exponents uniform in [e8m0_lo, e8m0_hi]: 2^-10 .. 2^-7
+    e8m0_hi: int = 120
     eps: float = 1e-6
 
     @property
@@ -74,18 +77,23 @@ class EngramConfig:
         """Same distributions, other sizes (for parity cases the oracle finishes quickly)."""
         return dataclasses.replace(self, **kw)
 
+    def row_bytes(self) -> int:
+        """Bytes of one table row with its scales: FP8 D + 4 (fp32 row scale),
+        FP8 with e8m0 blocks D + D/32, BF16 2D."""
+        if self.dtype == FP8:
+            return self.D + 4
+        if self.dtype == FP8_E8M0:
+            return self.D + self.D // 32
+        return 2 * self.D
+
     def table_bytes(self) -> int:
-        b = 1 if self.dtype == FP8 else 2
-        s = 4 if self.dtype == FP8 else 0
-        return sum(r * (self.D * b + s) for r in self.rows)
+        return sum(r * self.row_bytes() for r in self.rows)
 
     def algorithmic_bytes_per_token(self) -> int:
         """Bytes the fused lookup must move per token, with no cache credit:
-        3H rows (+ their fp32 scale for FP8), the 3H int32 row ids, and the four
-        bf16 streams read once and written once."""
-        b = 1 if self.dtype == FP8 else 2
-        s = 4 if self.dtype == FP8 else 0
-        return self.R * (self.D * b + s) + self.R * 4 + 2 * 4 * self.D * 2
+        3H rows (+ their scales), the 3H int32 row ids, and the four bf16 streams
+        read once and written once."""
+        return self.R * self.row_bytes() + self.R * 4 + 2 * 4 * self.D * 2
 
 
 CONFIGS = [
@@ -110,6 +118,10 @@ CONFIGS = [
     EngramConfig(name="packed_mm_fp8", seed=5, B=8, S=8192, vocab=129_280, n_eids=100_000,
                  H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8, ids="zipf", packed=True,
                  mean_sample_len=1024, image_span=256, image_frac=0.25),
+    # 6: full-size prefill with e8m0 block-scaled FP8 tables (the release's layout)
+    EngramConfig(name="full_prefill_fp8_e8m0", seed=6, B=8, S=8192, vocab=129_280,
+                 n_eids=100_000, H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8_E8M0, ids="zipf",
+                 repeat_frac=0.05),
 ]
 
 
@@ -229,8 +241,9 @@ def streams_host(cfg: EngramConfig, rank: int = 0) -> np.ndarray:
 
 def tables_host(cfg: EngramConfig):
     """Three tables on the host: (tables, scales).  FP8: uint8 [rows, D] from N(0,1)
-    clipped to +-448 + fp32 scales U[scale_lo, scale_hi]; BF16: uint16 bits from
-    N(0, bf16_std), scales None."""
+    clipped to +-448 + fp32 scales U[scale_lo, scale_hi]; FP8_E8M0: the same bytes
+    + uint8 e8m0 exponents [rows, D/32] uniform in [e8m0_lo, e8m0_hi]; BF16:
+    uint16 bits from N(0, bf16_std), scales None."""
     tabs, scales = [], []
     for n in range(3):
         g = rng(cfg, _K_TABLE, n)
@@ -239,6 +252,11 @@ def tables_host(cfg: EngramConfig):
             tabs.append(_to_e4m3_bytes(x))
             gs = rng(cfg, _K_SCALE, n)
             scales.append(gs.uniform(cfg.scale_lo, cfg.scale_hi, size=cfg.rows[n]).astype(np.float32))
+        elif cfg.dtype == FP8_E8M0:
+            tabs.append(_to_e4m3_bytes(x))
+            gs = rng(cfg, _K_SCALE, n)
+            scales.append(gs.integers(cfg.e8m0_lo, cfg.e8m0_hi + 1, size=(cfg.rows[n], cfg.D // 32),
+                                      dtype=np.int64).astype(np.uint8))
         else:
             tabs.append(_to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scales.append(None)
@@ -264,14 +282,15 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
     for n in range(3):
         rows = cfg.rows[n]
         g = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 7)
-        if cfg.dtype == FP8:
+        fp8 = cfg.dtype in (FP8, FP8_E8M0)
+        if fp8:
             t = torch.empty((rows, cfg.D), dtype=torch.uint8, device=device)
         else:
             t = torch.empty((rows, cfg.D), dtype=torch.int16, device=device)
         for r0 in range(0, rows, chunk_rows):
             r1 = min(rows, r0 + chunk_rows)
             x = torch.randn((r1 - r0, cfg.D), generator=g, device=device, dtype=torch.float32)
-            if cfg.dtype == FP8:
+            if fp8:
                 t[r0:r1] = x.clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
             else:
                 t[r0:r1] = x.mul_(cfg.bf16_std).to(torch.bfloat16).view(torch.int16)
@@ -281,6 +300,11 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
             gs = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 11)
             s = torch.rand((rows,), generator=gs, device=device, dtype=torch.float32)
             scales.append(s.mul_(cfg.scale_hi - cfg.scale_lo).add_(cfg.scale_lo))
+        elif cfg.dtype == FP8_E8M0:
+            gs = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 11)
+            scales.append(torch.randint(cfg.e8m0_lo, cfg.e8m0_hi + 1, (rows, cfg.D // 32),
+                                        generator=gs, device=device, dtype=torch.int32)
+                          .to(torch.uint8))
         else:
             scales.append(None)
     return tabs, scales
