@@ -4,9 +4,8 @@
 // One token per CTA of D/16 threads (16 columns each).  Thread 0 issues all 3H
 // row copies of the token at once (one contiguous D*elt-byte run per row, one
 // cp.async.bulk each) completing on a single mbarrier that expects their total
-// byte count (with the row's 32-column block exponents when the table has
-// them, one more bulk copy per row), while the other threads fetch the row
-// scales into shared memory
+// byte count, while the other threads fetch the row scales (or the rows'
+// 32-column block exponents, 16 coalesced bytes per thread) into shared memory
 // and, for large tokens, the four 32-byte stream slices into registers with
 // evict-first loads.  After the wait every thread reads its columns of the rows
 // from shared memory, accumulates the dequantised rows in fp32, the gate sums
@@ -136,7 +135,7 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
 
   // Thread 0: every row copy of the token on the one barrier.
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)R * (row_bytes + exp_bytes));
+    mbar_arrive_expect_tx(bar, (uint32_t)R * row_bytes);
     bool withhold = p.withhold != 0;
     for (int r = 0; r < R; ++r) {
       const int ni = (r >= H) + (r >= 2 * H);
@@ -146,14 +145,21 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
       }
       bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + (int64_t)ids[r] * row_bytes, row_bytes,
                bar);
-      if (kE8)
-        bulk_g2s(s_exps + (size_t)r * exp_bytes,
-                 static_cast<const uint8_t *>(p.scale[ni]) + (int64_t)ids[r] * exp_bytes, exp_bytes,
-                 bar);
     }
   }
   // Meanwhile: the row scales into shared memory, the stream slices into registers.
-  if (kFp8 && !kE8) {
+  if (kE8) {
+    // The rows' block exponents (D/32 bytes each, a multiple of 16 here), 16
+    // bytes per thread, coalesced: their latency overlaps the row copies.
+    const int per_row = (int)exp_bytes / 16;
+    for (int i = tid; i < R * per_row; i += blockDim.x) {
+      const int r = i / per_row, c = i - r * per_row;
+      const int ni = (r >= H) + (r >= 2 * H);
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+          static_cast<const uint8_t *>(p.scale[ni]) + (int64_t)ids[r] * exp_bytes) + c);
+      *reinterpret_cast<uint4 *>(s_exps + (size_t)r * exp_bytes + 16 * c) = v;
+    }
+  } else if (kFp8) {
     for (int r = tid; r < R; r += blockDim.x) {
       const int ni = (r >= H) + (r >= 2 * H);
       s_scale[r] = __ldg(static_cast<const float *>(p.scale[ni]) + ids[r]);
