@@ -201,6 +201,8 @@ class Step:
         self.hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
         self.out = torch.empty_like(d["streams"])
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.primes = (eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0]
+                       if cfg.hash_vocab else None)
         self.launches = 3
 
     def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None):
@@ -212,7 +214,7 @@ class Step:
                            stream=self.stream, dead=d["dead"])
         eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
                        row_ids_out=self.rows, status=self.status, stream=self.stream,
-                       positions=d["positions"])
+                       positions=d["positions"], primes=self.primes)
         if ev_start is not None:
             ev_start.record(self.stream)
         eg.engram_lookup_fused(self.rows, cfg.H, d["tables"], x, d["alpha"], cfg.eps,
@@ -406,7 +408,11 @@ def oracle_sample(cfg, d, n_tokens):
         e, _ = oracle.compress_masked(ids, tid2eid, cfg.n_eids, dead)
     else:
         e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
-    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
+    if cfg.hash_vocab:
+        r, _ = oracle.hash_bucketed(e, cfg.H, oracle.bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0],
+                                    history=hist, positions=pos)
+    else:
+        r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
     r = r.reshape(n, -1)
     # full-size host copies are too large: the oracle gets tables holding only the
     # rows the sample needs, with the row ids remapped onto them
@@ -439,7 +445,11 @@ def time_oracle(cfg, s, repeats=1):
             e, _ = oracle.compress_masked(s["ids"], s["tid2eid"], cfg.n_eids, s["dead"])
         else:
             e, _ = oracle.compress(s["ids"], s["tid2eid"], cfg.n_eids)
-        oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"], positions=s.get("positions"))
+        if cfg.hash_vocab:
+            oracle.hash_bucketed(e, cfg.H, oracle.bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0],
+                                 history=s["hist"], positions=s.get("positions"))
+        else:
+            oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"], positions=s.get("positions"))
         oracle.lookup(s["remap"], cfg.H, oracle_dtype(cfg), s["tables"], s["scales"], s["x"],
                       s["alpha"], cfg.eps)
     return (time.perf_counter() - t0) / repeats
@@ -469,7 +479,11 @@ def reference_sample(cfg, n):
         e, _ = oracle.compress_masked(ids, tid2eid, cfg.n_eids, dead)
     else:
         e, _ = oracle.compress(ids, tid2eid, cfg.n_eids)
-    r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
+    if cfg.hash_vocab:
+        r, _ = oracle.hash_bucketed(e, cfg.H, oracle.bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0],
+                                    history=hist, positions=pos)
+    else:
+        r, _ = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, positions=pos)
     r = r.reshape(n, -1)
     g = np.random.default_rng([cfg.seed, 99])
     tabs, scs, remap = [], [], np.empty_like(r)

@@ -47,11 +47,15 @@ def _load():
     L.engram_hash.argtypes = [vp, i32, i32, vp, vp, i32, C.POINTER(C.c_int64), vp, vp, vp]
     L.engram_hash_packed.argtypes = [vp, i32, i32, vp, vp, vp, i32, C.POINTER(C.c_int64), vp, vp,
                                      vp]
+    L.engram_hash_bucketed.argtypes = [vp, i32, i32, vp, vp, vp, i32, C.POINTER(C.c_int64), vp, vp,
+                                       vp]
+    L.engram_bucket_primes.argtypes = [i32, i32, i32, i64, C.POINTER(C.c_int64)]
     L.engram_lookup_fused.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, vp, vp,
                                       C.c_float, vp, vp, vp, vp]
     L.engram_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
     for f in ("engram_compress", "engram_compress_masked", "engram_hash", "engram_hash_packed",
-              "engram_lookup_fused", "engram_read_status"):
+              "engram_hash_bucketed", "engram_bucket_primes", "engram_lookup_fused",
+              "engram_read_status"):
         getattr(L, f).restype = C.c_int32
     L.engram_status_string.argtypes = [C.c_int32]
     L.engram_status_string.restype = C.c_char_p
@@ -163,10 +167,24 @@ def engram_compress(token_ids, tid2eid, n_eids: int, eids_out=None, status=None,
     return eids_out
 
 
+def engram_bucket_primes(n_layers: int, max_ngram: int, n_heads: int, hash_vocab: int):
+    """The released layout's bucket sizes, [n_layers][max_ngram - 1][n_heads] (host ints)."""
+    n = n_layers * (max_ngram - 1) * n_heads
+    out = (C.c_int64 * n)()
+    _check(lib.engram_bucket_primes(n_layers, max_ngram, n_heads, hash_vocab, out),
+           "engram_bucket_primes")
+    flat = list(out)
+    k = max_ngram - 1
+    return [[flat[(l * k + i) * n_heads:(l * k + i + 1) * n_heads] for i in range(k)]
+            for l in range(n_layers)]
+
+
 def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_ids_out=None,
-                status=None, stream=None, positions=None):
+                status=None, stream=None, positions=None, primes=None):
     """Row ids [B, S, 3, n_heads] int32 for eids [B, S]; history/history_out [B, 3];
-    positions [B, S] (optional): each token's index within its packed sample."""
+    positions [B, S] (optional): each token's index within its packed sample.
+    With primes ([3][n_heads] bucket sizes of one layer) the ids index one table
+    cut into prime buckets (engram_hash_bucketed) and rows is not used."""
     import torch
     _need(eids, (torch.int32,), "eids")
     if eids.dim() != 2:
@@ -178,6 +196,13 @@ def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_id
     _need(history, (torch.int32,), "history")
     _need(history_out, (torch.int32,), "history_out")
     _need(positions, (torch.int32,), "positions")
+    if primes is not None:
+        flat = [int(v) for order in primes for v in order]
+        pr = (C.c_int64 * len(flat))(*flat)
+        _check(lib.engram_hash_bucketed(_ptr(eids), B, S, _ptr(positions), _ptr(history),
+                                        _ptr(history_out), n_heads, pr, _ptr(row_ids_out),
+                                        _ptr(status), _stream(stream)), "engram_hash_bucketed")
+        return row_ids_out
     r = (C.c_int64 * 3)(*[int(x) for x in rows])
     _check(lib.engram_hash_packed(_ptr(eids), B, S, _ptr(positions), _ptr(history),
                                   _ptr(history_out), n_heads, r, _ptr(row_ids_out), _ptr(status),

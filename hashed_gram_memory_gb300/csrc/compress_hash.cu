@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
           h ^= h >> 29;
         }
       }
-      p.row_ids[t * R + r] = (int32_t)mod_by_reciprocal(h, p.rows[ni], p.rmul[ni]);
+      p.row_ids[t * R + r] =
+          (int32_t)(p.off[ni][j] + mod_by_reciprocal(h, p.mod[ni][j], p.rmul[ni][j]));
     }
   }
   flag_warp(p.status, flags);

@@ -133,39 +133,40 @@ ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tok
                                 status, stream);
 }
 
-ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, int32_t seq,
-                                            const int32_t *positions, const int32_t *history,
-                                            int32_t *history_out, int32_t n_heads,
-                                            const int64_t *rows_host, int32_t *row_ids_out,
-                                            int32_t *status, void *stream) {
-  if (batch < 0 || seq < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: batch or seq < 0");
+// Shared validation and launch of the hash: mod/off are the per-(order, head)
+// modulus and offset of every row id (host arrays of 3 * n_heads).
+static engram_status hash_common(const char *fn, const int32_t *eids, int32_t batch, int32_t seq,
+                                 const int32_t *positions, const int32_t *history,
+                                 int32_t *history_out, int32_t n_heads, const int64_t *mod,
+                                 const int64_t *off, int32_t *row_ids_out, int32_t *status,
+                                 void *stream) {
+  if (batch < 0 || seq < 0) return fail(ENGRAM_ERR_INVALID_ARG, "%s: batch or seq < 0", fn);
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: n_heads must be in [1, %d]", ENGRAM_MAX_HEADS);
-  if (!rows_host) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows_host is NULL");
-  for (int n = 0; n < 3; ++n)
-    if (rows_host[n] < 1 || rows_host[n] > INT32_MAX)
-      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows[%d] must be in [1, 2^31-1]", n);
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
+  for (int r = 0; r < 3 * n_heads; ++r)
+    if (mod[r] < 1 || off[r] < 0 || off[r] + mod[r] - 1 > INT32_MAX)
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: row ids must fit [0, 2^31-1] (bucket %d)", fn, r);
   const int64_t T = (int64_t)batch * seq;
   const size_t R = 3 * (size_t)n_heads;
   if (T > 0 && (!eids || !row_ids_out))
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: eids or row_ids_out is NULL");
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: eids or row_ids_out is NULL", fn);
   if (!aligned(eids, 4) || !aligned(history, 4) || !aligned(history_out, 4) ||
       !aligned(row_ids_out, 4) || !aligned(status, 4))
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: int32 pointers must be 4-byte aligned");
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: int32 pointers must be 4-byte aligned", fn);
   if (overlap(eids, T * 4, row_ids_out, T * R * 4))
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: row_ids_out overlaps eids");
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids_out overlaps eids", fn);
   if (history_out) {
     const size_t hb = (size_t)batch * 3 * 4;
     if (overlap(history_out, hb, eids, T * 4) || overlap(history_out, hb, row_ids_out, T * R * 4))
-      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: history_out overlaps eids or row_ids_out");
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: history_out overlaps eids or row_ids_out", fn);
     if (history && history != history_out && overlap(history, hb, history_out, hb))
-      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: history and history_out overlap partially");
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: history and history_out overlap partially", fn);
   }
   if (history && overlap(history, (size_t)batch * 12, row_ids_out, T * R * 4))
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: row_ids_out overlaps history");
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids_out overlaps history", fn);
   if (positions && (!aligned(positions, 4) || overlap(positions, T * 4, row_ids_out, T * R * 4) ||
                     (history_out && overlap(positions, T * 4, history_out, (size_t)batch * 12))))
-    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: positions misaligned or overlapping outputs");
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: positions misaligned or overlapping outputs", fn);
   if (T == 0 && (!history_out || batch == 0)) return ok();
   engram_status st = check_device();
   if (st != ENGRAM_OK) return st;
@@ -181,12 +182,92 @@ ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, 
   p.batch = batch;
   p.seq = seq;
   p.H = n_heads;
-  for (int n = 0; n < 3; ++n) {
-    p.rows[n] = (uint64_t)rows_host[n];
-    p.rmul[n] = UINT64_MAX / p.rows[n];
-    for (int j = 0; j < n_heads; ++j) p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
-  }
+  for (int n = 0; n < 3; ++n)
+    for (int j = 0; j < n_heads; ++j) {
+      const int r = n * n_heads + j;
+      p.mod[n][j] = (uint64_t)mod[r];
+      p.off[n][j] = (uint64_t)off[r];
+      p.rmul[n][j] = UINT64_MAX / p.mod[n][j];
+      p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
+    }
   return launched("engram_hash launch", engram::launch_hash(p, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, int32_t seq,
+                                            const int32_t *positions, const int32_t *history,
+                                            int32_t *history_out, int32_t n_heads,
+                                            const int64_t *rows_host, int32_t *row_ids_out,
+                                            int32_t *status, void *stream) {
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: n_heads must be in [1, %d]",
+                ENGRAM_MAX_HEADS);
+  if (!rows_host) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows_host is NULL");
+  int64_t mod[3 * ENGRAM_MAX_HEADS], off[3 * ENGRAM_MAX_HEADS];
+  for (int n = 0; n < 3; ++n) {
+    if (rows_host[n] < 1 || rows_host[n] > INT32_MAX)
+      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: rows[%d] must be in [1, 2^31-1]", n);
+    for (int j = 0; j < n_heads; ++j) {
+      mod[n * n_heads + j] = rows_host[n];
+      off[n * n_heads + j] = 0;
+    }
+  }
+  return hash_common("engram_hash", eids, batch, seq, positions, history, history_out, n_heads,
+                     mod, off, row_ids_out, status, stream);
+}
+
+ENGRAM_API engram_status engram_hash_bucketed(const int32_t *eids, int32_t batch, int32_t seq,
+                                              const int32_t *positions, const int32_t *history,
+                                              int32_t *history_out, int32_t n_heads,
+                                              const int64_t *primes_host, int32_t *row_ids_out,
+                                              int32_t *status, void *stream) {
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash_bucketed: n_heads must be in [1, %d]",
+                ENGRAM_MAX_HEADS);
+  if (!primes_host) return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash_bucketed: primes is NULL");
+  int64_t off[3 * ENGRAM_MAX_HEADS];
+  int64_t sum = 0;
+  for (int r = 0; r < 3 * n_heads; ++r) {
+    if (primes_host[r] < 1 || primes_host[r] > INT32_MAX)
+      return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash_bucketed: bucket %d size out of range", r);
+    off[r] = sum;
+    sum += primes_host[r];
+  }
+  if (sum - 1 > INT32_MAX)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash_bucketed: %lld rows exceed 2^31-1",
+                (long long)sum);
+  return hash_common("engram_hash_bucketed", eids, batch, seq, positions, history, history_out,
+                     n_heads, primes_host, off, row_ids_out, status, stream);
+}
+
+// Trial division: no divisor d with d*d <= n.
+static bool is_prime_u64(int64_t n) {
+  if (n < 2) return false;
+  if (n % 2 == 0) return n == 2;
+  for (int64_t d = 3; d * d <= n; d += 2)
+    if (n % d == 0) return false;
+  return true;
+}
+
+ENGRAM_API engram_status engram_bucket_primes(int32_t n_layers, int32_t max_ngram, int32_t n_heads,
+                                              int64_t hash_vocab, int64_t *primes_out_host) {
+  if (n_layers < 1 || max_ngram < 2 || n_heads < 1 || hash_vocab < 1 || !primes_out_host)
+    return fail(ENGRAM_ERR_INVALID_ARG, "engram_bucket_primes: bad arguments");
+  if ((int64_t)n_layers * (max_ngram - 1) * n_heads > 65536)
+    return fail(ENGRAM_ERR_UNSUPPORTED, "engram_bucket_primes: more than 65536 buckets");
+  int64_t k = 0;
+  for (int32_t l = 0; l < n_layers; ++l)
+    for (int32_t n = 2; n <= max_ngram; ++n) {
+      int64_t c = hash_vocab;  // every order starts again at the vocabulary
+      for (int32_t j = 0; j < n_heads; ++j) {
+        for (;; ++c) {
+          bool taken = false;
+          for (int64_t q = 0; q < k && !taken; ++q) taken = primes_out_host[q] == c;
+          if (!taken && is_prime_u64(c)) break;
+        }
+        primes_out_host[k++] = c++;
+      }
+    }
+  return ok();
 }
 
 ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t seq,

@@ -35,8 +35,11 @@ struct HashParams {
   int32_t batch, seq, H;
   int32_t tokens_per_block;  // tokens whose 3H outputs one block owns
   int32_t history_inline;    // 1: seq == 1 and the block writes history_out itself
-  uint64_t rows[3];
-  uint64_t rmul[3];  // floor((2^64 - 1) / rows[n]): the reciprocal for h mod rows[n]
+  // Row r = (n-2)*H + j of a token is off[n-2][j] + (h mod mod[n-2][j]):
+  // one table per order (off 0, mod rows_n) or one table cut into prime buckets.
+  uint64_t mod[3][kMaxHeads];
+  uint64_t off[3][kMaxHeads];
+  uint64_t rmul[3][kMaxHeads];  // floor((2^64 - 1) / mod): the reciprocal for h mod mod
   uint64_t seed[3][kMaxHeads];
 };
 

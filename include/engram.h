@@ -186,6 +186,37 @@ ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, 
                                             int32_t *status, void *stream);
 
 /*
+ * engram_bucket_primes -- the released table layout's bucket sizes (VeOmni PR
+ * page: "n-gram memory lookup" commit, the bucket layout reproduces the
+ * release's prime draw, giving 384006168 / 384016682 rows for its two Engram
+ * layers; the commit on hash_vocab_size: primes drawn above the hash vocabulary;
+ * the review on validate_bucket_layout: 462 for 1 layer, max n-gram 4, 2 heads,
+ * vocabulary 64).  For every layer, every order n = 2..max_ngram and every head,
+ * in that order, the smallest prime >= hash_vocab, counting up from the last
+ * prime of the same order, that no earlier bucket took; every order starts
+ * again from hash_vocab.  Host-only: writes n_layers * (max_ngram-1) * n_heads
+ * int64 primes to primes_out_host in draw order (at most 65536).
+ */
+ENGRAM_API engram_status engram_bucket_primes(int32_t n_layers, int32_t max_ngram, int32_t n_heads,
+                                              int64_t hash_vocab, int64_t *primes_out_host);
+
+/*
+ * engram_hash_bucketed -- engram_hash_packed into one table cut into prime
+ * buckets (the released layout): the bucket of order n and head j has
+ * primes_host[(n-2)*n_heads + j] rows and starts after the buckets before it in
+ * that order; its row id is offset + (h mod prime).  primes_host: host int64
+ * [3 * n_heads] (one layer's orders 2..4 from engram_bucket_primes); their sum
+ * must be <= 2^31 - 1 and at most the table's rows.  For engram_lookup_fused,
+ * pass that one table as table[0..2] (with its scales) and its rows as
+ * rows[0..2].
+ */
+ENGRAM_API engram_status engram_hash_bucketed(const int32_t *eids, int32_t batch, int32_t seq,
+                                              const int32_t *positions, const int32_t *history,
+                                              int32_t *history_out, int32_t n_heads,
+                                              const int64_t *primes_host, int32_t *row_ids_out,
+                                              int32_t *status, void *stream);
+
+/*
  * engram_lookup_fused -- gather + dequantise the 3*n_heads rows of every token,
  * average them into m, gate with g = sigmoid(<rmsnorm(stream0), rmsnorm(m)> /
  * sqrt(D)) and add g * alpha_s * m into the four mHC streams (VeOmni PR page:

@@ -52,6 +52,11 @@ def lib():
         L.orc_hash_packed.restype = C.c_int
         L.orc_hash_packed.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
                                       C.c_int32, C.POINTER(C.c_int64), C.c_void_p, C.c_void_p]
+        L.orc_bucket_primes.restype = C.c_int
+        L.orc_bucket_primes.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_void_p]
+        L.orc_hash_bucketed.restype = C.c_int
+        L.orc_hash_bucketed.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                        C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p]
         L.orc_hash.restype = C.c_int
         L.orc_hash.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_void_p, C.c_int32,
                                C.POINTER(C.c_int64), C.c_void_p, C.c_void_p]
@@ -140,6 +145,32 @@ def hash_ids(eids, n_heads: int, rows, history=None, want_history: bool = False,
     hout = np.full((B, 3), fill, dtype=np.int32) if want_history else None
     r = (C.c_int64 * 3)(*[int(x) for x in rows])
     flags = lib().orc_hash_packed(_p(e), B, S, _p(pos), _p(hist), n_heads, r, _p(out), _p(hout))
+    if want_history:
+        return out, hout, int(flags)
+    return out, int(flags)
+
+
+def bucket_primes(n_layers: int, max_ngram: int, n_heads: int, hash_vocab: int) -> np.ndarray:
+    """[n_layers, max_ngram - 1, n_heads] int64 primes of the bucket layout."""
+    out = np.zeros(n_layers * (max_ngram - 1) * n_heads, np.int64)
+    flags = lib().orc_bucket_primes(n_layers, max_ngram, n_heads, hash_vocab, _p(out))
+    assert flags == 0
+    return out.reshape(n_layers, max_ngram - 1, n_heads)
+
+
+def hash_bucketed(eids, n_heads: int, primes, history=None, positions=None,
+                  want_history: bool = False, fill: int = -7):
+    """Row ids [B, S, 3, H] into one prime-bucketed table (primes [3, H] of one layer)."""
+    e = _c(eids, np.int32)
+    B, S = e.shape
+    hist = None if history is None else _c(history, np.int32).reshape(B, 3)
+    pos = None if positions is None else _c(positions, np.int32).reshape(B, S)
+    pr = _c(primes, np.int64).reshape(-1)
+    assert pr.size == 3 * n_heads
+    out = np.full((B, S, 3, n_heads), fill, dtype=np.int32)
+    hout = np.full((B, 3), fill, dtype=np.int32) if want_history else None
+    flags = lib().orc_hash_bucketed(_p(e), B, S, _p(pos), _p(hist), n_heads, _p(pr), _p(out),
+                                    _p(hout))
     if want_history:
         return out, hout, int(flags)
     return out, int(flags)

@@ -269,6 +269,94 @@ int orc_hash(const int32_t *eids, int32_t B, int32_t S, const int32_t *history,
   return orc_hash_packed(eids, B, S, NULL, history, n_heads, rows, row_ids_out, history_out);
 }
 
+/* n is prime: trial division by every d with d*d <= n. */
+static int orc_is_prime(int64_t n) {
+  if (n < 2) return 0;
+  for (int64_t d = 2; d * d <= n; ++d)
+    if (n % d == 0) return 0;
+  return 1;
+}
+
+/*
+ * The released prime-bucket layout (VeOmni PR page, "n-gram memory lookup"
+ * commit: the bucket layout reproduces the release's prime draw by trial
+ * division; the commit on hash_vocab_size: the primes are drawn above the hash
+ * vocabulary; the review on validate_bucket_layout: a table needs at least the
+ * sum of its layer's primes).  For every layer, every order n = 2..max_ngram and
+ * every head j, in that order: the smallest prime >= hash_vocab + (the heads
+ * already drawn for this order) that no earlier bucket uses; each order starts
+ * again from hash_vocab.  primes_out gets n_layers * (max_ngram - 1) * n_heads
+ * primes in draw order.
+ */
+int orc_bucket_primes(int32_t n_layers, int32_t max_ngram, int32_t n_heads, int64_t hash_vocab,
+                      int64_t *primes_out) {
+  if (n_layers < 1 || max_ngram < 2 || n_heads < 1 || hash_vocab < 1) return ORC_BAD_ARG;
+  const int64_t total = (int64_t)n_layers * (max_ngram - 1) * n_heads;
+  int64_t k = 0;
+  for (int32_t l = 0; l < n_layers; ++l)
+    for (int32_t n = 2; n <= max_ngram; ++n) {
+      int64_t cand = hash_vocab - 1;
+      for (int32_t j = 0; j < n_heads; ++j) {
+        ++cand;
+        for (;;) {
+          int used = 0;
+          for (int64_t q = 0; q < k && !used; ++q) used = primes_out[q] == cand;
+          if (!used && orc_is_prime(cand)) break;
+          ++cand;
+        }
+        primes_out[k++] = cand;
+      }
+    }
+  return k == total ? 0 : ORC_BAD_ARG;
+}
+
+/*
+ * Hash ids into one table cut into prime buckets: the bucket of order n, head j
+ * (r = (n-2)*H + j) has primes[r] rows and starts at the sum of the buckets
+ * before it in draw order; row = offset_r + (h mod primes[r]), h the n-gram hash
+ * of orc_hash_packed's blocked window.  Dead tokens, flags and history_out as in
+ * orc_hash_packed.
+ */
+int orc_hash_bucketed(const int32_t *eids, int32_t B, int32_t S, const int32_t *positions,
+                      const int32_t *history, int32_t n_heads, const int64_t *primes,
+                      int32_t *row_ids_out, int32_t *history_out) {
+  if (B < 0 || S < 0 || n_heads < 1) return ORC_BAD_ARG;
+  const int R = 3 * n_heads;
+  for (int r = 0; r < R; ++r)
+    if (primes[r] < 1) return ORC_BAD_ARG;
+  const int64_t T = (int64_t)B * S;
+  int flags = 0;
+#pragma omp parallel for schedule(static) reduction(| : flags)
+  for (int64_t t = 0; t < T; ++t) {
+    int32_t b = (int32_t)(t / S), s = (int32_t)(t % S);
+    int32_t w4[4];
+    int st = orc_window(eids, S, positions, history, b, s, w4);
+    if (st == ORC_BAD_EID) {
+      flags |= ORC_BAD_EID;
+      continue;
+    }
+    int64_t offset = 0;
+    for (int r = 0; r < R; ++r) {
+      int n = 2 + r / n_heads, j = r % n_heads;
+      if (st == 1) {
+        row_ids_out[t * R + r] = ORC_DEAD;
+      } else {
+        uint64_t h = orc_ngram_hash(w4 + (4 - n), n, j);
+        row_ids_out[t * R + r] = (int32_t)(offset + (int64_t)(h % (uint64_t)primes[r]));
+      }
+      offset += primes[r];
+    }
+  }
+  if (history_out) {
+    for (int32_t b = 0; b < B; ++b) {
+      int32_t tail[3];
+      for (int k = 0; k < 3; ++k) tail[k] = orc_eid_at(eids, S, history, b, S - 3 + k);
+      for (int k = 0; k < 3; ++k) history_out[(int64_t)b * 3 + k] = tail[k];
+    }
+  }
+  return flags;
+}
+
 /*
  * The fused lookup for n_tokens tokens, one at a time, in fp64:
  *  1. gather + dequantise the 3H rows of the token: FP8 byte decoded exactly,

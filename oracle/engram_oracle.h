@@ -61,6 +61,13 @@ int orc_hash_packed(const int32_t *eids, int32_t B, int32_t S, const int32_t *po
                     const int32_t *history, int32_t n_heads, const int64_t rows[3],
                     int32_t *row_ids_out, int32_t *history_out);
 
+int orc_bucket_primes(int32_t n_layers, int32_t max_ngram, int32_t n_heads, int64_t hash_vocab,
+                      int64_t *primes_out);
+
+int orc_hash_bucketed(const int32_t *eids, int32_t B, int32_t S, const int32_t *positions,
+                      const int32_t *history, int32_t n_heads, const int64_t *primes,
+                      int32_t *row_ids_out, int32_t *history_out);
+
 int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
                int32_t D, const void *const tables[3], const void *const scales[3],
                const int64_t rows[3], const uint16_t *streams_in, const float *alpha,

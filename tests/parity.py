@@ -45,6 +45,11 @@ def host_inputs(cfg: W.EngramConfig, rank: int = 0) -> HostInputs:
                       scales, W.streams_host(cfg, rank), W.alpha(cfg), pos, dead)
 
 
+def layer_primes(cfg: W.EngramConfig):
+    """The bucket sizes [3][H] of one layer's table (the oracle's draw)."""
+    return oracle.bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0]
+
+
 def oracle_dtype(cfg: W.EngramConfig) -> int:
     return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.BF16: oracle.BF16}[cfg.dtype]
 
@@ -55,8 +60,12 @@ def oracle_path(inp: HostInputs):
         eids, f1 = oracle.compress_masked(inp.ids, inp.tid2eid, cfg.n_eids, inp.dead)
     else:
         eids, f1 = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
-    rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history, want_history=True,
-                                     positions=inp.positions)
+    if cfg.hash_vocab:
+        rows, hist, f2 = oracle.hash_bucketed(eids, cfg.H, layer_primes(cfg), history=inp.history,
+                                              positions=inp.positions, want_history=True)
+    else:
+        rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history,
+                                         want_history=True, positions=inp.positions)
     y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H, oracle_dtype(cfg), inp.tables,
                                 inp.scales, inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha,
                                 cfg.eps, aux=True)
@@ -98,8 +107,9 @@ def gpu_path(cfg: W.EngramConfig, dev: dict, aux: bool = True, in_place: bool = 
     hist_out = None
     if dev["history"] is not None:
         hist_out = torch.empty_like(dev["history"])
+    primes = eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0] if cfg.hash_vocab else None
     rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=dev["history"], history_out=hist_out,
-                          status=status, positions=dev.get("positions"))
+                          status=status, positions=dev.get("positions"), primes=primes)
     gate = torch.full((cfg.T,), float("nan"), device="cuda") if aux else None
     mem = torch.full((cfg.T, cfg.D), float("nan"), device="cuda") if aux else None
     x = dev["streams"]

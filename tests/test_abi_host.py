@@ -127,3 +127,14 @@ def test_python_binding_rejects_cpu_tensors(eg):
     import torch
     with pytest.raises(eg.EngramError):
         eg.engram_compress(torch.zeros(4, dtype=torch.int32), torch.zeros(4, dtype=torch.int32), 3)
+
+
+def test_library_bucket_primes_match_oracle_and_pages(eg):
+    """engram_bucket_primes is host code: its draw must equal the oracle's and give
+    the pages' row counts (384006168 / 384016682; 462)."""
+    import oracle
+    lib_p = eg.engram_bucket_primes(2, 4, 8, 16_000_000)
+    assert [sum(sum(o) for o in layer) for layer in lib_p] == [384006168, 384016682]
+    assert sum(sum(o) for o in eg.engram_bucket_primes(1, 4, 2, 64)[0]) == 462
+    for args in [(2, 4, 8, 16_000_000), (1, 4, 3, 1000), (3, 5, 2, 97)]:
+        assert (oracle.bucket_primes(*args).tolist() == eg.engram_bucket_primes(*args))

@@ -32,8 +32,9 @@ def run_full(eg, cfg, device_inputs):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     eids = eg.engram_compress(d["ids"], d["tid2eid"], cfg.n_eids, status=st, dead=d["dead"])
     hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
+    primes = eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0] if cfg.hash_vocab else None
     rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=d["history"], history_out=hist_out,
-                          status=st, positions=d["positions"])
+                          status=st, positions=d["positions"], primes=primes)
     out = torch.empty_like(d["streams"])
     eg.engram_lookup_fused(rows, cfg.H, d["tables"], d["streams"], d["alpha"], cfg.eps,
                            streams_out=out, status=st)
@@ -57,7 +58,7 @@ def device_inputs(eg, cfg):
                 tables=eg.Tables(dt, tabs, scales))
 
 
-@pytest.mark.parametrize("ci", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("ci", [1, 2, 3, 4, 5, 6, 7])
 def test_full_size_sampled(eg, ci):
     import torch
     cfg = W.CONFIGS[ci]
@@ -78,8 +79,12 @@ def test_full_size_sampled(eg, ci):
         e_ref, f1 = oracle.compress(ids_h, d["tid2eid"].cpu().numpy(), cfg.n_eids)
     hist_h = None if d["history"] is None else d["history"].cpu().numpy()
     pos_h = None if d["positions"] is None else d["positions"].cpu().numpy()
-    r_ref, h_ref, f2 = oracle.hash_ids(e_ref, cfg.H, cfg.rows, history=hist_h, want_history=True,
-                                       positions=pos_h)
+    if cfg.hash_vocab:
+        r_ref, h_ref, f2 = oracle.hash_bucketed(e_ref, cfg.H, P.layer_primes(cfg), history=hist_h,
+                                                positions=pos_h, want_history=True)
+    else:
+        r_ref, h_ref, f2 = oracle.hash_ids(e_ref, cfg.H, cfg.rows, history=hist_h,
+                                           want_history=True, positions=pos_h)
     assert f1 == f2 == 0
     assert np.array_equal(eids.cpu().numpy(), e_ref)
     assert np.array_equal(rows.cpu().numpy(), r_ref)

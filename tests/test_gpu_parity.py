@@ -32,6 +32,11 @@ SMALL = {
     "e8m0_loud_h4_d1024": C[6].scaled(B=1, S=233, H=4, D=1024, rows=(1009, 1013, 1019),
                                       e8m0_lo=124, e8m0_hi=129),
     "e8m0_d96": C[6].scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41)),
+    "release_layout_d256": C[7].scaled(B=2, S=333, rows=(32_000,) * 3, hash_vocab=1000),
+    "release_layout_d512_h4": C[7].scaled(B=1, S=301, H=4, D=512, rows=(16_000,) * 3,
+                                          hash_vocab=1000, e8m0_lo=124, e8m0_hi=129),
+    "release_layout_bf16_d1024": C[7].scaled(B=1, S=129, H=4, D=1024, rows=(16_000,) * 3,
+                                             hash_vocab=1000, dtype=W.BF16),
     "packed_mm_loud_h4": C[5].scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
                                      scale_hi=1.0, mean_sample_len=40, image_span=8,
                                      image_frac=0.4),

@@ -635,3 +635,69 @@ def test_e8m0_uniform_blocks_equal_row_scales():
     y1, g1, m1, _ = oracle.lookup(ids, 3, oracle.FP8_E8M0, tabs, blocks, x, alpha, 1e-6, aux=True)
     y2, g2, m2, _ = oracle.lookup(ids, 3, oracle.FP8, tabs, rows_scale, x, alpha, 1e-6, aux=True)
     assert (y1 == y2).all() and (g1 == g2).all() and (m1 == m2).all()
+
+
+# ----------------------------------------------------------------- prime buckets
+
+def _bucket_golden():
+    out = []
+    with open(os.path.join(GOLDEN, "bucket_layout_pages.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            left, right = line.split(":")
+            out.append(([int(v) for v in left.split()], [int(v) for v in right.split()]))
+    return out
+
+
+def test_bucket_primes_reproduce_the_pages_row_counts():
+    for (layers, max_n, heads, vocab), sums in _bucket_golden():
+        primes = oracle.bucket_primes(layers, max_n, heads, vocab)
+        assert primes.sum(axis=(1, 2)).tolist() == sums
+
+
+def test_bucket_primes_are_distinct_primes_above_the_vocab():
+    sympy = pytest.importorskip("sympy")
+    primes = oracle.bucket_primes(2, 4, 8, 16_000_000)
+    flat = primes.reshape(-1).tolist()
+    assert len(set(flat)) == len(flat) and min(flat) >= 16_000_000
+    assert all(sympy.isprime(int(p)) for p in flat)
+    # each order starts again from the vocabulary: the first head of every order
+    # of layer 0 takes the smallest prime not yet used
+    assert flat[0] == sympy.nextprime(16_000_000 - 1)
+
+
+def test_bucketed_rows_land_in_their_bucket_at_h_mod_p():
+    """row = offset_r + (h mod p_r), offsets the running sum of the buckets in
+    draw order; h from an independent Python-int restatement of the fold."""
+    def sm(x):
+        z = (x + 0x9E3779B97F4A7C15) & M64
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+        return z ^ (z >> 31)
+    H = 3
+    primes = oracle.bucket_primes(1, 4, H, 1000)[0]           # [3, H]
+    offsets = np.concatenate([[0], np.cumsum(primes.reshape(-1))[:-1]]).reshape(3, H)
+    g = np.random.default_rng(40)
+    eids = g.integers(1, 5000, size=(2, 9)).astype(np.int32)
+    got, flags = oracle.hash_bucketed(eids, H, primes)
+    assert flags == 0
+    for b in range(2):
+        seq = [0, 0, 0] + [int(v) for v in eids[b]]
+        for s in range(9):
+            for n in (2, 3, 4):
+                for j in range(H):
+                    h = sm(n * 16 + j)
+                    for e in seq[s + 4 - n: s + 4]:
+                        h = ((h ^ e) * FOLD) & M64
+                        h ^= h >> 29
+                    assert got[b, s, n - 2, j] == offsets[n - 2, j] + h % int(primes[n - 2, j])
+
+
+def test_bucketed_hash_keeps_dead_and_packed_rules():
+    primes = oracle.bucket_primes(1, 4, 2, 10_000)[0]
+    e = np.array([[5, 6, oracle.DEAD, 7, 8, 9]], np.int32)
+    got, _ = oracle.hash_bucketed(e, 2, primes)
+    assert (got[0, 2] == oracle.DEAD).all()
+    fresh, _ = oracle.hash_bucketed(e[:, 3:], 2, primes)
+    assert (got[0, 3:] == fresh[0]).all()

@@ -63,6 +63,9 @@ class EngramConfig:
     scale_hi: float = 1e-2
     e8m0_lo: int = 117     # block exponents uniform in [e8m0_lo, e8m0_hi]: 2^-10 .. 2^-7
     e8m0_hi: int = 120
+    # The released layout: one table of rows[0] rows cut into prime buckets drawn
+    # above hash_vocab (0: one table per n-gram order)
+    hash_vocab: int = 0
     eps: float = 1e-6
 
     @property
@@ -87,6 +90,8 @@ class EngramConfig:
         return 2 * self.D
 
     def table_bytes(self) -> int:
+        if self.hash_vocab:
+            return self.rows[0] * self.row_bytes()
         return sum(r * self.row_bytes() for r in self.rows)
 
     def algorithmic_bytes_per_token(self) -> int:
@@ -118,10 +123,16 @@ CONFIGS = [
     EngramConfig(name="packed_mm_fp8", seed=5, B=8, S=8192, vocab=129_280, n_eids=100_000,
                  H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8, ids="zipf", packed=True,
                  mean_sample_len=1024, image_span=256, image_frac=0.25),
-    # 6: full-size prefill with e8m0 block-scaled FP8 tables (the release's layout)
+    # 6: full-size prefill with e8m0 block-scaled FP8 tables (the release's dequantisation)
     EngramConfig(name="full_prefill_fp8_e8m0", seed=6, B=8, S=8192, vocab=129_280,
                  n_eids=100_000, H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8_E8M0, ids="zipf",
                  repeat_frac=0.05),
+    # 7: the released table layout: one Engram layer's table of 384,006,168 rows
+    #    of 256 FP8 values with (1, 32) e8m0 blocks (98 GB), cut into 24 prime
+    #    buckets (orders 2..4 x 8 heads) drawn above a 16,000,000 hash vocabulary
+    EngramConfig(name="release_layout_fp8", seed=7, B=8, S=8192, vocab=129_280, n_eids=100_000,
+                 H=8, D=256, rows=(384_006_168,) * 3, dtype=FP8_E8M0, ids="zipf",
+                 repeat_frac=0.05, hash_vocab=16_000_000),
 ]
 
 
@@ -245,7 +256,7 @@ def tables_host(cfg: EngramConfig):
     + uint8 e8m0 exponents [rows, D/32] uniform in [e8m0_lo, e8m0_hi]; BF16:
     uint16 bits from N(0, bf16_std), scales None."""
     tabs, scales = [], []
-    for n in range(3):
+    for n in range(1 if cfg.hash_vocab else 3):
         g = rng(cfg, _K_TABLE, n)
         x = g.standard_normal((cfg.rows[n], cfg.D), dtype=np.float32)
         if cfg.dtype == FP8:
@@ -260,6 +271,8 @@ def tables_host(cfg: EngramConfig):
         else:
             tabs.append(_to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scales.append(None)
+    if cfg.hash_vocab:   # one table, shared by the three orders
+        tabs, scales = tabs * 3, scales * 3
     return tabs, scales
 
 
@@ -279,7 +292,7 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
     [rows] scales (None for BF16)."""
     import torch
     tabs, scales = [], []
-    for n in range(3):
+    for n in range(1 if cfg.hash_vocab else 3):
         rows = cfg.rows[n]
         g = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 7)
         fp8 = cfg.dtype in (FP8, FP8_E8M0)
@@ -307,6 +320,8 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
                           .to(torch.uint8))
         else:
             scales.append(None)
+    if cfg.hash_vocab:   # one table, shared by the three orders
+        tabs, scales = tabs * 3, scales * 3
     return tabs, scales
 
 
