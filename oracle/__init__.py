@@ -65,6 +65,11 @@ def lib():
                                  C.c_void_p * 3, C.c_void_p * 3, C.POINTER(C.c_int64),
                                  C.c_void_p, C.c_void_p, C.c_double, C.c_void_p, C.c_void_p,
                                  C.c_void_p]
+        L.orc_connection.restype = C.c_int
+        L.orc_connection.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32,
+                                     C.c_void_p * 3, C.c_void_p * 3, C.POINTER(C.c_int64),
+                                     C.c_void_p, C.c_int32, C.c_void_p, C.c_void_p, C.c_double,
+                                     C.c_void_p, C.c_void_p, C.c_void_p]
         L.orc_num_threads.restype = C.c_int
         _lib = L
     return _lib
@@ -204,6 +209,34 @@ def lookup(row_ids, n_heads: int, dtype: int, tables, scales, streams, alpha, ep
     if aux:
         return y, g, m, int(flags)
     return y, int(flags)
+
+
+def connection(row_ids, n_heads: int, dtype: int, tables, scales, wkv, streams, alpha, eps: float,
+               rows=None, fill: int = 0xDEAD):
+    """The wkv connection: rows concatenated per token, projected by wkv [D, K]
+    (bf16 bits), gated and added into the streams [T, 4, D].  Returns
+    (streams_out, gate [T], k [T, D], flags)."""
+    ids = _c(row_ids, np.int32)
+    x = _c(streams, np.uint16)
+    D = x.shape[-1]
+    T = x.size // (4 * D)
+    tabs = [_c(t, np.uint16 if dtype == BF16 else np.uint8) for t in tables]
+    d = tabs[0].shape[1]
+    scs = [(_c(s, np.uint8) if s is not None else None) for s in scales] if scales else [None] * 3
+    w = _c(wkv, np.uint16)
+    assert w.shape == (D, 3 * n_heads * d)
+    if rows is None:
+        rows = [t.shape[0] for t in tabs]
+    a = _c(alpha, np.float32)
+    y = np.full(x.shape, fill, dtype=np.uint16)
+    g = np.full(T, np.nan)
+    k = np.full((T, D), np.nan)
+    tp = (C.c_void_p * 3)(*[t.ctypes.data for t in tabs])
+    sp = (C.c_void_p * 3)(*[(s.ctypes.data if s is not None else None) for s in scs])
+    r = (C.c_int64 * 3)(*[int(v) for v in rows])
+    flags = lib().orc_connection(_p(ids), T, n_heads, dtype, d, tp, sp, r, _p(w), D, _p(x), _p(a),
+                                 float(eps), _p(y), _p(g), _p(k))
+    return y, g, k, int(flags)
 
 
 def bf16_bits_to_float(bits) -> np.ndarray:

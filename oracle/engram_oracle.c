@@ -463,6 +463,96 @@ int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_
   return flags;
 }
 
+/*
+ * The Engram connection with a wkv projection (VeOmni PR page, "n-gram memory
+ * lookup" commit and the layer commit: the other half of Engram, wkv and the
+ * gate, reads the mHC streams; the rows cross to it as n-gram embeddings).  The
+ * pages give no shapes or formula; the reading implemented here: per token,
+ *  1. e = the 3H dequantised rows of width d concatenated in (order, head)
+ *     order, K = 3H*d values (FP8 with e8m0 blocks or BF16: exact in bf16);
+ *  2. k = wkv e, wkv bf16 [D, K] (row j holds output j's weights), in fp64;
+ *  3. g = sigmoid(<rmsnorm(stream0), rmsnorm(k)> / sqrt(D)), the spec's gate
+ *     with k in place of the mean;
+ *  4. out_s = bf16_round(stream_s + g * alpha_s * k), rounded once.
+ * Bad rows and dead tokens as in orc_lookup.  gate_out [n_tokens] and k_out
+ * [n_tokens, D] are optional.
+ */
+int orc_connection(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
+                   int32_t d, const void *const tables[3], const void *const scales[3],
+                   const int64_t rows[3], const uint16_t *wkv, int32_t D,
+                   const uint16_t *streams_in, const float *alpha, double eps,
+                   uint16_t *streams_out, double *gate_out, double *k_out) {
+  if (n_tokens < 0 || n_heads < 1 || d < 1 || D < 1) return ORC_BAD_ARG;
+  if (dtype != ORC_BF16 && dtype != ORC_FP8_E8M0_B32) return ORC_BAD_ARG;
+  if (dtype == ORC_FP8_E8M0_B32 && d % 32) return ORC_BAD_ARG;
+  const int R = 3 * n_heads;
+  const int64_t K = (int64_t)R * d;
+  int flags = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : flags)
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int32_t *ids = row_ids + t * R;
+    int bad = 0, dead = 0;
+    for (int r = 0; r < R; ++r) {
+      if (ids[r] == ORC_DEAD)
+        ++dead;
+      else if (ids[r] < 0 || (int64_t)ids[r] >= rows[r / n_heads])
+        bad = 1;
+    }
+    if (bad || (dead && dead != R)) {
+      flags |= ORC_BAD_ROW;
+      continue;
+    }
+    const uint16_t *x = streams_in + t * 4 * (int64_t)D;
+    uint16_t *y = streams_out + t * 4 * (int64_t)D;
+    if (dead) {
+      if (y != x) memcpy(y, x, (size_t)4 * D * sizeof(uint16_t));
+      if (gate_out) gate_out[t] = 0.0;
+      if (k_out)
+        for (int i = 0; i < D; ++i) k_out[t * D + i] = 0.0;
+      continue;
+    }
+    double *e = (double *)malloc((size_t)K * sizeof(double));
+    double *k = (double *)calloc((size_t)D, sizeof(double));
+    for (int r = 0; r < R; ++r) {
+      const int n = r / n_heads;
+      const int64_t row = ids[r];
+      for (int i = 0; i < d; ++i) {
+        double v;
+        if (dtype == ORC_FP8_E8M0_B32)
+          v = orc_e4m3fn_decode(((const uint8_t *)tables[n])[row * d + i]) *
+              orc_e8m0_decode(((const uint8_t *)scales[n])[row * (d / 32) + i / 32]);
+        else
+          v = orc_bf16_decode(((const uint16_t *)tables[n])[row * d + i]);
+        e[(int64_t)r * d + i] = v;
+      }
+    }
+    for (int j = 0; j < D; ++j) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < K; ++i) acc += orc_bf16_decode(wkv[(int64_t)j * K + i]) * e[i];
+      k[j] = acc;
+    }
+    double saa = 0.0, skk = 0.0, sak = 0.0;
+    for (int i = 0; i < D; ++i) {
+      double a = orc_bf16_decode(x[i]);
+      saa += a * a;
+      skk += k[i] * k[i];
+      sak += a * k[i];
+    }
+    double logit = sak / (sqrt(saa / D + eps) * sqrt(skk / D + eps) * sqrt((double)D));
+    double g = 1.0 / (1.0 + exp(-logit));
+    for (int s = 0; s < 4; ++s)
+      for (int i = 0; i < D; ++i)
+        y[(int64_t)s * D + i] =
+            orc_bf16_round(orc_bf16_decode(x[(int64_t)s * D + i]) + g * (double)alpha[s] * k[i]);
+    if (gate_out) gate_out[t] = g;
+    if (k_out)
+      for (int i = 0; i < D; ++i) k_out[t * D + i] = k[i];
+    free(e);
+    free(k);
+  }
+  return flags;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

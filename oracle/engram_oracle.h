@@ -73,6 +73,12 @@ int orc_lookup(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_
                const int64_t rows[3], const uint16_t *streams_in, const float *alpha,
                double eps, uint16_t *streams_out, double *gate_out, double *mem_out);
 
+int orc_connection(const int32_t *row_ids, int64_t n_tokens, int32_t n_heads, int32_t dtype,
+                   int32_t d, const void *const tables[3], const void *const scales[3],
+                   const int64_t rows[3], const uint16_t *wkv, int32_t D,
+                   const uint16_t *streams_in, const float *alpha, double eps,
+                   uint16_t *streams_out, double *gate_out, double *k_out);
+
 int orc_num_threads(void);
 
 #ifdef __cplusplus

@@ -701,3 +701,77 @@ def test_bucketed_hash_keeps_dead_and_packed_rules():
     assert (got[0, 2] == oracle.DEAD).all()
     fresh, _ = oracle.hash_bucketed(e[:, 3:], 2, primes)
     assert (got[0, 3:] == fresh[0]).all()
+
+
+# ----------------------------------------------------------------- wkv connection
+
+def _connection_case(seed, T=7, H=2, d=64, D=96, rows=(13, 17, 19), dtype=oracle.FP8_E8M0):
+    g = np.random.default_rng(seed)
+    if dtype == oracle.FP8_E8M0:
+        tabs = [W._to_e4m3_bytes(g.standard_normal((r, d)).astype(np.float32) * 4) for r in rows]
+        scs = [g.integers(118, 130, size=(r, d // 32)).astype(np.uint8) for r in rows]
+    else:
+        tabs = [W._to_bf16_bits(g.standard_normal((r, d)).astype(np.float32)) for r in rows]
+        scs = None
+    ids = np.stack([g.integers(0, rows[r // H], size=T) for r in range(3 * H)], 1).astype(np.int32)
+    wkv = W._to_bf16_bits((g.standard_normal((D, 3 * H * d)) * 0.05).astype(np.float32))
+    x = W._to_bf16_bits(g.standard_normal((T, 4, D)).astype(np.float32))
+    alpha = g.standard_normal(4).astype(np.float32)
+    return tabs, scs, ids, wkv, x, alpha
+
+
+def _decoded_concat(tabs, scs, ids, H, dtype):
+    parts = []
+    for r in range(ids.shape[1]):
+        n = r // H
+        if dtype == oracle.FP8_E8M0:
+            v = torch.from_numpy(tabs[n]).view(torch.float8_e4m3fn).double().numpy()[ids[:, r]]
+            sc = torch.from_numpy(scs[n]).view(torch.float8_e8m0fnu).double().numpy()[ids[:, r]]
+            parts.append(v * np.repeat(sc, 32, axis=1))
+        else:
+            parts.append(torch.from_numpy(tabs[n].view(np.int16)).view(torch.bfloat16).double()
+                         .numpy()[ids[:, r]])
+    return np.concatenate(parts, axis=1)
+
+
+@pytest.mark.parametrize("dtype", [oracle.FP8_E8M0, oracle.BF16])
+def test_connection_projection_matches_numpy_matmul(dtype):
+    """k = wkv @ concat(rows), checked with torch's decodes and NumPy's matmul."""
+    H = 2
+    tabs, scs, ids, wkv, x, alpha = _connection_case(1, H=H, dtype=dtype)
+    _, gate, k, flags = oracle.connection(ids, H, dtype, tabs, scs, wkv, x, alpha, 1e-6)
+    assert flags == 0
+    e = _decoded_concat(tabs, scs, ids, H, dtype)
+    w = torch.from_numpy(wkv.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.allclose(k, e @ w.T, rtol=1e-12, atol=1e-12)
+    a = oracle.bf16_bits_to_float(x[:, 0, :]).astype(np.float64)
+    cos = np.einsum("td,td->t", a, k) / (np.linalg.norm(a, axis=1) * np.linalg.norm(k, axis=1))
+    _, g0, _, _ = oracle.connection(ids, H, dtype, tabs, scs, wkv, x, alpha, 0.0)
+    assert np.allclose(g0, 1 / (1 + np.exp(-cos * math.sqrt(a.shape[1]))), rtol=1e-12)
+
+
+def test_connection_identity_weights_give_the_concatenated_rows():
+    H, d = 1, 32
+    tabs, scs, ids, _, _, alpha = _connection_case(2, H=H, d=d, D=3 * d)
+    wkv = W._to_bf16_bits(np.eye(3 * d, dtype=np.float32))
+    x = W._to_bf16_bits(np.random.default_rng(2).standard_normal((ids.shape[0], 4, 3 * d))
+                        .astype(np.float32))
+    _, _, k, _ = oracle.connection(ids, H, oracle.FP8_E8M0, tabs, scs, wkv, x, alpha, 1e-6)
+    assert (k == _decoded_concat(tabs, scs, ids, H, oracle.FP8_E8M0)).all()
+
+
+def test_connection_gate_half_and_dead_pass_through():
+    H, d, D = 1, 32, 64
+    tabs, scs, ids, wkv, x, alpha = _connection_case(3, H=H, d=d, D=D)
+    # k constant over the columns (equal weight rows) and stream 0 summing to zero: g = 1/2
+    wkv = np.tile(wkv[:1], (D, 1))
+    xf = np.random.default_rng(3).standard_normal((ids.shape[0], 4, D)).astype(np.float32)
+    xf[:, 0, :] = np.tile(np.array([0.75, -0.75], np.float32), D // 2)
+    x = W._to_bf16_bits(xf)
+    ids = ids.copy()
+    ids[4] = oracle.DEAD
+    y, gate, k, flags = oracle.connection(ids, H, oracle.FP8_E8M0, tabs, scs, wkv, x, alpha, 1e-6)
+    assert flags == 0
+    live = [t for t in range(ids.shape[0]) if t != 4]
+    assert np.all(gate[live] == 0.5)
+    assert (y[4] == x[4]).all() and gate[4] == 0
