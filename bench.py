@@ -68,7 +68,7 @@ def config_of(name: str, args=None) -> W.EngramConfig:
 
 
 def workload_desc(cfg: W.EngramConfig) -> dict:
-    return {
+    d = {
         "workload": cfg.name,
         "batch": cfg.B, "seq": cfg.S, "tokens_per_step": cfg.T, "hash_heads": cfg.H, "D": cfg.D,
         "table_rows": list(cfg.rows), "table_dtype": cfg.dtype,
@@ -76,9 +76,17 @@ def workload_desc(cfg: W.EngramConfig) -> dict:
         "repeated_4gram_frac": cfg.repeat_frac, "decode_history": cfg.decode,
         "l2": "no flush: every input is larger than the 129 MB L2 "
               f"(tables {cfg.table_bytes() / 2**30:.1f} GiB, streams "
-              f"{cfg.T * 4 * cfg.D * 2 / 1e9:.2f} GB in + out per step)",
+              f"{cfg.T * 4 * cfg.width * 2 / 1e9:.2f} GB in + out per step)",
         "parallelism": "replicas (weak scaling, no data-path collective)",
     }
+    if cfg.hidden:
+        d.update({"path": "connection: rows concatenated (K = 3H*D), k = wkv e on the tensor "
+                          "cores, gate and add into the streams",
+                  "hidden": cfg.hidden, "K": cfg.K, "wkv": f"bf16 [{cfg.hidden}, {cfg.K}]"})
+    return d
+
+
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 
 
 def measured_peaks():
@@ -90,11 +98,23 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s sustained under the power cap (the projection runs inside
+    a seconds-long loop of steps)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured"
+    return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
 def recorded_traffic(cfg, kernel: str):
     """Per-launch DRAM bytes of the lookup kernel from the committed ncu summary,
     scaled by tokens, or None when the kernel timed is not the one captured or its
     sources changed since the capture."""
-    if kernel not in ("auto", "bulk") or not os.path.exists(TRAFFIC_FILE):
+    if kernel not in ("auto", "bulk", "gemm") or not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
@@ -186,6 +206,7 @@ def device_inputs(eg, cfg, rank, device):
         streams=W.streams_device(cfg, device, rank),
         alpha=torch.from_numpy(W.alpha(cfg)).to(device),
         tables=eg.Tables(dt, tabs, scales),
+        wkv=W.wkv_device(cfg, device) if cfg.hidden else None,
     )
 
 
@@ -204,6 +225,11 @@ class Step:
         self.primes = (eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0]
                        if cfg.hash_vocab else None)
         self.launches = 3
+        if cfg.hidden:   # the connection: concat rows, project, gate + add
+            self.e = torch.empty((cfg.T, cfg.K), dtype=torch.bfloat16, device=dev)
+            self.state = torch.empty((cfg.T,), dtype=torch.uint8, device=dev)
+            self.k = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
+            self.launches = 5
 
     def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None):
         eg, cfg, d = self.eg, self.cfg, self.d
@@ -215,6 +241,18 @@ class Step:
         eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
                        row_ids_out=self.rows, status=self.status, stream=self.stream,
                        positions=d["positions"], primes=self.primes)
+        if cfg.hidden:
+            eg.engram_concat_rows(self.rows, cfg.H, d["tables"], e_out=self.e,
+                                  state_out=self.state, status=self.status, stream=self.stream)
+            if ev_start is not None:
+                ev_start.record(self.stream)
+            eg.engram_wkv_project(self.e, d["wkv"], k_out=self.k, status=self.status,
+                                  stream=self.stream)
+            if ev_end is not None:
+                ev_end.record(self.stream)
+            eg.engram_gate_add(self.k, self.state, x, d["alpha"], cfg.eps, streams_out=out,
+                               stream=self.stream)
+            return
         if ev_start is not None:
             ev_start.record(self.stream)
         eg.engram_lookup_fused(self.rows, cfg.H, d["tables"], x, d["alpha"], cfg.eps,
@@ -282,20 +320,44 @@ def run_native(args):
         clocks.stop()
 
     # engram_forward_host takes no dead mask or positions: no e2e leg for packed batches
-    e2e = None if (args.no_e2e or cfg.packed) else run_e2e(eg, cfg, step, stream, args.e2e_steps,
-                                                           world, device)
+    if args.no_e2e or cfg.packed:
+        e2e = None
+    elif cfg.hidden:
+        e2e = run_e2e_connection(eg, cfg, step, stream, args.e2e_steps, world, device)
+    else:
+        e2e = run_e2e(eg, cfg, step, stream, args.e2e_steps, world, device)
     cpu = None if (args.no_cpu_baseline or rank != 0) else cpu_baseline(cfg, d, args.cpu_sample_tokens)
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
         n_dead = int(d["dead"].sum().item()) if d["dead"] is not None else 0
         # a dead token moves its row ids and a copy of its streams, no table rows
-        bytes_dead = cfg.R * 4 + 2 * 4 * cfg.D * 2
+        bytes_dead = cfg.R * 4 + 2 * 4 * cfg.width * 2
         bytes_tok = (cfg.algorithmic_bytes_per_token() * (cfg.T - n_dead) + bytes_dead * n_dead) / cfg.T
         lk = statistics.mean(lookup_ms)
         achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
         traffic = recorded_traffic(cfg, args.lookup_kernel)
         value = whole_job_throughput(world * cfg.T * K, ms_total * 1e-3)
+        if cfg.hidden:
+            tpeak, tpeak_kind = measured_tensor_peak()
+            flops = cfg.connection_flops_per_token() * (cfg.T - n_dead)
+            t_ach = flops / (lk * 1e-3) / 1e12
+            roof = {
+                "kernel": "engram_wkv_project (wkv_gemm_kernel)",
+                "bound": "tensor",
+                "achieved": t_ach,
+                "peak": tpeak,
+                "peak_source": f"{tpeak_kind} (MEASURED_PEAKS.json bf16_tflops_sustained: "
+                               "cuBLAS bf16 back to back under the power cap)",
+                "unit": "TFLOP/s",
+                "frac": t_ach / tpeak,
+                "traffic": recorded_traffic(cfg, "gemm"),
+                "algorithmic_flops_per_token": cfg.connection_flops_per_token(),
+                "flops_per_launch": flops,
+                "gemm_shape": [cfg.T, cfg.hidden, cfg.K],
+                "projection_ms_mean": lk,
+                "projection_ms_median": statistics.median(lookup_ms),
+            }
         line = {
             "metric": METRIC,
             "value": value,
@@ -307,11 +369,11 @@ def run_native(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
+            "dtype": "bf16 x bf16 -> f32 (tensor cores)" if cfg.hidden else "f32",
             "data": "synthetic (seeded; tables and streams generated on the GPU)",
             "config": workload_desc(cfg),
             "hbm_gbs_effective_step": bytes_tok * cfg.T * K / (ms_total * 1e-3) / 1e9,
-            "roofline": {
+            "roofline": roof if cfg.hidden else {
                 "kernel": "engram_lookup_fused",
                 "lookup_kernel": args.lookup_kernel,
                 "bound": "hbm",
@@ -383,6 +445,52 @@ def run_e2e(eg, cfg, step, stream, steps, world, device):
                    "copy streams; host timer around the steps + a final stream sync"}
 
 
+def run_e2e_connection(eg, cfg, step, stream, steps, world, device):
+    """The connection through the public API with HOST buffers: every step copies
+    the token ids and the four input streams from pinned host memory to the
+    device, runs compress, hash and the connection's three calls, and copies the
+    updated streams back to pinned host memory, all inside the timed region."""
+    import torch
+    from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
+    d = step.d
+    ids_h = d["ids"].cpu().pin_memory()
+    x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    x_h.copy_(d["streams"])
+    y_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    ids_d = torch.empty_like(d["ids"])
+    x_d = torch.empty_like(d["streams"])
+    y_d = torch.empty_like(d["streams"])
+
+    def one():
+        with torch.cuda.stream(stream):
+            ids_d.copy_(ids_h, non_blocking=True)
+            x_d.copy_(x_h, non_blocking=True)
+            step(ids=ids_d, x=x_d, out=y_d)
+            y_h.copy_(y_d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    stream.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    stream.synchronize()
+    dt = time.perf_counter() - t0
+    dt = max_over_ranks(dt, device)
+    ok = torch.equal(y_h.to(device), step.out)
+    h2d = ids_h.numel() * 4 + x_h.numel() * 2
+    d2h = y_h.numel() * 2
+    return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "matches_device_step": bool(ok),
+            "how": "pinned host ids + streams copied in, compress / hash / concat / projection / "
+                   "gate + add, streams copied out, one stream, not overlapped; host timer "
+                   "around the steps + a final stream sync"}
+
+
 # ----------------------------------------------------------------- CPU oracle
 
 def oracle_sample(cfg, d, n_tokens):
@@ -395,6 +503,11 @@ def oracle_sample(cfg, d, n_tokens):
         ids = d["ids"][:n].cpu().numpy()
         hist = d["history"][:n].cpu().numpy()
         x = d["streams"][:n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.D)
+    elif cfg.hidden:   # the first n tokens of sequence 0 (their windows start at position 0)
+        n = min(n_tokens, cfg.S)
+        ids = d["ids"][:1, :n].cpu().numpy()
+        hist = None
+        x = d["streams"][0, :n].cpu().numpy().view(np.uint16).reshape(n, 4, cfg.width)
     else:
         nseq = max(1, min(cfg.B, -(-n_tokens // cfg.S)))   # whole sequences: windows self-contained
         n = nseq * cfg.S
@@ -427,8 +540,10 @@ def oracle_sample(cfg, d, n_tokens):
         host_tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
         host_scales.append(d["tables"].scales[k].index_select(0, idx).cpu().numpy()
                            if cfg.dtype != W.BF16 else None)
+    wkv = d["wkv"].cpu().numpy().view(np.uint16) if cfg.hidden else None
     return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=x, tables=host_tabs, scales=host_scales,
-                remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n, dead=dead, positions=pos)
+                remap=remap, rows=r, alpha=d["alpha"].cpu().numpy(), n=n, dead=dead, positions=pos,
+                wkv=wkv)
 
 
 def oracle_dtype(cfg):
@@ -450,20 +565,32 @@ def time_oracle(cfg, s, repeats=1):
                                  history=s["hist"], positions=s.get("positions"))
         else:
             oracle.hash_ids(e, cfg.H, cfg.rows, history=s["hist"], positions=s.get("positions"))
-        oracle.lookup(s["remap"], cfg.H, oracle_dtype(cfg), s["tables"], s["scales"], s["x"],
-                      s["alpha"], cfg.eps)
+        if cfg.hidden:
+            oracle.connection(s["remap"], cfg.H, oracle_dtype(cfg), s["tables"], s["scales"],
+                              s["wkv"], s["x"], s["alpha"], cfg.eps)
+        else:
+            oracle.lookup(s["remap"], cfg.H, oracle_dtype(cfg), s["tables"], s["scales"], s["x"],
+                          s["alpha"], cfg.eps)
     return (time.perf_counter() - t0) / repeats
+
+
+CONNECTION_CPU_SAMPLE = 4096
 
 
 def cpu_baseline(cfg, d, n_tokens):
     import oracle
+    if cfg.hidden:
+        n_tokens = min(n_tokens, CONNECTION_CPU_SAMPLE)
     s = oracle_sample(cfg, d, n_tokens)
     dt = time_oracle(cfg, s)
+    what = ("compress + hash + connection (concatenated rows, wkv projection, gate, add)"
+            if cfg.hidden else "compress + hash + fused lookup")
+    where = "of sequence 0" if cfg.hidden else "(whole sequences)"
     return {"value": s["n"] / dt, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"first {s['n']} tokens (whole sequences) of the {cfg.name} batch (same seeded inputs, the "
-                      f"rows they need copied from the device): compress + hash + fused lookup in "
-                      f"the fp64 C oracle, {dt:.2f} s wall"}
+            "sample": f"first {s['n']} tokens {where} of the {cfg.name} batch (same seeded "
+                      f"inputs, the rows they need copied from the device): {what} in the fp64 "
+                      f"C oracle, {dt:.2f} s wall"}
 
 
 def reference_sample(cfg, n):
@@ -503,9 +630,9 @@ def reference_sample(cfg, n):
         else:
             tabs.append(W._to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scs.append(None)
-    return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=W.streams_host(sub).reshape(n, 4, cfg.D),
+    return dict(ids=ids, hist=hist, tid2eid=tid2eid, x=W.streams_host(sub).reshape(n, 4, cfg.width),
                 tables=tabs, scales=scs, remap=remap, alpha=W.alpha(cfg), n=n, dead=dead,
-                positions=pos)
+                positions=pos, wkv=W.wkv_host(cfg) if cfg.hidden else None)
 
 
 def run_reference(args, budget_s: float = 60.0):
@@ -538,8 +665,10 @@ def run_reference(args, budget_s: float = 60.0):
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"each step: {n} of the {cfg.T} tokens of {cfg.name} through the "
-                                   "fp64 C oracle (compress + hash + fused lookup), with tables "
-                                   "holding the rows those tokens need"},
+                                   "fp64 C oracle (compress + hash + "
+                                   + ("connection with the wkv projection" if cfg.hidden
+                                      else "fused lookup")
+                                   + "), with tables holding the rows those tokens need"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -83,6 +83,17 @@ def _load():
     L.engram_forward_static.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
                                         C.POINTER(engram_tables), vp, vp, vp, C.c_float, vp, vp]
     L.engram_forward_static.restype = i32
+    L.engram_connection_workspace_bytes.argtypes = [i64, i32, i32, i32]
+    L.engram_connection_workspace_bytes.restype = sz
+    L.engram_connection.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, i32, vp, vp, vp,
+                                    C.c_float, vp, sz, vp, vp, vp, vp]
+    L.engram_connection.restype = i32
+    L.engram_concat_rows.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, vp, vp, vp]
+    L.engram_concat_rows.restype = i32
+    L.engram_wkv_project.argtypes = [vp, i64, i32, vp, i32, vp, vp, vp]
+    L.engram_wkv_project.restype = i32
+    L.engram_gate_add.argtypes = [vp, vp, i64, i32, vp, vp, vp, C.c_float, vp, vp]
+    L.engram_gate_add.restype = i32
     return L
 
 
@@ -235,6 +246,113 @@ def engram_lookup_fused(row_ids, n_heads: int, tables: Tables, streams_in, alpha
                                    _ptr(streams_out), _ptr(alpha), float(eps), _ptr(gate_out),
                                    _ptr(mem_out), _ptr(status), _stream(stream)),
            "engram_lookup_fused")
+    return streams_out
+
+
+def engram_connection_workspace_bytes(n_tokens: int, n_heads: int, d: int, D: int) -> int:
+    return int(lib.engram_connection_workspace_bytes(n_tokens, n_heads, d, D))
+
+
+def engram_connection(row_ids, n_heads: int, tables: Tables, wkv, streams_in, alpha,
+                      eps: float = 1e-6, streams_out=None, workspace=None, gate_out=None,
+                      k_out=None, status=None, stream=None):
+    """The connection with a wkv projection: rows concatenated, k = wkv e, gate, add.
+    wkv: bf16 [D, 3*n_heads*d]; streams_in: bf16 [..., 4, D]; returns streams_out."""
+    import torch
+    _need(row_ids, (torch.int32,), "row_ids")
+    bf = (torch.bfloat16, torch.int16)
+    _need(streams_in, bf, "streams_in")
+    _need(wkv, bf, "wkv")
+    _need(alpha, (torch.float32,), "alpha")
+    D = streams_in.shape[-1]
+    if streams_in.shape[-2] != 4:
+        raise EngramError(ERR_INVALID_ARG, "streams_in must be [..., 4, D]")
+    T = streams_in.numel() // (4 * D)
+    if row_ids.numel() != T * 3 * n_heads:
+        raise EngramError(ERR_INVALID_ARG, "row_ids and streams disagree on the token count")
+    if tuple(wkv.shape) != (D, 3 * n_heads * tables.D):
+        raise EngramError(ERR_INVALID_ARG, f"wkv must be [{D}, {3 * n_heads * tables.D}]")
+    if streams_out is None:
+        streams_out = torch.empty_like(streams_in)
+    _need(streams_out, bf, "streams_out")
+    _need(gate_out, (torch.float32,), "gate_out")
+    _need(k_out, (torch.float32,), "k_out")
+    need = engram_connection_workspace_bytes(T, n_heads, tables.D, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=streams_in.device)
+    s = tables.struct()
+    _check(lib.engram_connection(_ptr(row_ids), T, n_heads, C.byref(s), _ptr(wkv), D,
+                                 _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
+                                 _ptr(workspace), workspace.numel(), _ptr(gate_out), _ptr(k_out),
+                                 _ptr(status), _stream(stream)),
+           "engram_connection")
+    return streams_out
+
+
+def engram_concat_rows(row_ids, n_heads: int, tables: Tables, e_out=None, state_out=None,
+                       status=None, stream=None):
+    """E = the tokens' concatenated rows (bf16 [T, 3*n_heads*d]) and their state
+    (uint8 [T]: 0 live, 1 dead, 2 bad).  Returns (E, state)."""
+    import torch
+    _need(row_ids, (torch.int32,), "row_ids")
+    T = row_ids.numel() // (3 * n_heads)
+    K = 3 * n_heads * tables.D
+    dev = row_ids.device
+    if e_out is None:
+        e_out = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+    if state_out is None:
+        state_out = torch.empty((T,), dtype=torch.uint8, device=dev)
+    _need(e_out, (torch.bfloat16, torch.int16), "e_out")
+    _need(state_out, (torch.uint8,), "state_out")
+    if e_out.numel() != T * K or state_out.numel() != T:
+        raise EngramError(ERR_INVALID_ARG, "e_out / state_out sizes")
+    s = tables.struct()
+    _check(lib.engram_concat_rows(_ptr(row_ids), T, n_heads, C.byref(s), _ptr(e_out),
+                                  _ptr(state_out), _ptr(status), _stream(stream)),
+           "engram_concat_rows")
+    return e_out, state_out
+
+
+def engram_wkv_project(e, wkv, k_out=None, status=None, stream=None):
+    """k = E wkv^T on the tensor cores: e bf16 [T, K], wkv bf16 [D, K] -> k fp32 [T, D]."""
+    import torch
+    bf = (torch.bfloat16, torch.int16)
+    _need(e, bf, "e")
+    _need(wkv, bf, "wkv")
+    T, K = e.shape
+    D = wkv.shape[0]
+    if wkv.shape[1] != K:
+        raise EngramError(ERR_INVALID_ARG, "e and wkv disagree on K")
+    if k_out is None:
+        k_out = torch.empty((T, D), dtype=torch.float32, device=e.device)
+    _need(k_out, (torch.float32,), "k_out")
+    if k_out.numel() != T * D:
+        raise EngramError(ERR_INVALID_ARG, "k_out must be [T, D]")
+    _check(lib.engram_wkv_project(_ptr(e), T, K, _ptr(wkv), D, _ptr(k_out), _ptr(status),
+                                  _stream(stream)), "engram_wkv_project")
+    return k_out
+
+
+def engram_gate_add(k, state, streams_in, alpha, eps: float = 1e-6, streams_out=None,
+                    gate_out=None, stream=None):
+    """The gate of k against stream 0 and the gated add into the four streams."""
+    import torch
+    _need(k, (torch.float32,), "k")
+    _need(state, (torch.uint8,), "state")
+    bf = (torch.bfloat16, torch.int16)
+    _need(streams_in, bf, "streams_in")
+    _need(alpha, (torch.float32,), "alpha")
+    D = streams_in.shape[-1]
+    T = streams_in.numel() // (4 * D)
+    if k.numel() != T * D or state.numel() != T:
+        raise EngramError(ERR_INVALID_ARG, "k / state sizes disagree with the streams")
+    if streams_out is None:
+        streams_out = torch.empty_like(streams_in)
+    _need(streams_out, bf, "streams_out")
+    _need(gate_out, (torch.float32,), "gate_out")
+    _check(lib.engram_gate_add(_ptr(k), _ptr(state), T, D, _ptr(streams_in), _ptr(streams_out),
+                               _ptr(alpha), float(eps), _ptr(gate_out), _stream(stream)),
+           "engram_gate_add")
     return streams_out
 
 

@@ -374,6 +374,158 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
                   engram::launch_lookup(p, tb.dtype, (cudaStream_t)stream));
 }
 
+static size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+ENGRAM_API size_t engram_connection_workspace_bytes(int64_t n_tokens, int32_t n_heads, int32_t d,
+                                                    int32_t D) {
+  if (n_tokens < 0 || n_heads < 1 || d < 1 || D < 1) return 0;
+  const size_t T = (size_t)n_tokens, K = 3 * (size_t)n_heads * d;
+  return round256(T * K * 2) + round256(T * (size_t)D * 4) + round256(T);
+}
+
+static engram_status check_connection_tables(const char *fn, int32_t n_heads,
+                                             const engram_tables *tables_host) {
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
+  if (!tables_host) return fail(ENGRAM_ERR_INVALID_ARG, "%s: tables is NULL", fn);
+  const engram_tables &tb = *tables_host;
+  if (tb.dtype != ENGRAM_TABLE_BF16 && tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+    return fail(ENGRAM_ERR_UNSUPPORTED,
+                "%s: the projection takes BF16 or FP8 + e8m0 tables (exact in bf16)", fn);
+  if (tb.D < 32 || tb.D % 32 != 0 || tb.D > 65536)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: row width %d must be a multiple of 32", fn, tb.D);
+  for (int n = 0; n < 3; ++n) {
+    if (tb.rows[n] < 1 || tb.rows[n] > INT32_MAX || !tb.table[n] || !aligned(tb.table[n], 16))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: table[%d] bad (rows, NULL or alignment)", fn, n);
+    if (tb.dtype != ENGRAM_TABLE_BF16 && !tb.scale[n])
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: scale[%d] is NULL", fn, n);
+  }
+  return ENGRAM_OK;
+}
+
+static engram_status check_projection(const char *fn, int64_t K, int32_t D) {
+  if (K < 64 || K > INT32_MAX || D < 256 || D > 8192 || !engram::wkv_gemm_supported(D, (int)K))
+    return fail(ENGRAM_ERR_UNSUPPORTED,
+                "%s: D must be a multiple of 256 in [256, 8192] and K (= 3*n_heads*d) of 64", fn);
+  return ENGRAM_OK;
+}
+
+static engram_status check_gate_add(const char *fn, int64_t n_tokens, int32_t D,
+                                    const uint16_t *streams_in, uint16_t *streams_out,
+                                    const float *alpha, float eps, float *gate_out) {
+  if (!alpha || !aligned(alpha, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: alpha NULL or misaligned", fn);
+  if (!(eps >= 0.f) || !isfinite(eps))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", fn);
+  if (n_tokens == 0) return ENGRAM_OK;
+  if (!streams_in || !streams_out || !aligned(streams_in, 16) || !aligned(streams_out, 16) ||
+      !aligned(gate_out, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: NULL or misaligned stream or gate buffer", fn);
+  const size_t sbytes = (size_t)n_tokens * 4 * D * 2;
+  if (streams_in != streams_out && overlap(streams_in, sbytes, streams_out, sbytes))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: streams_out overlaps streams_in partially", fn);
+  return ENGRAM_OK;
+}
+
+ENGRAM_API engram_status engram_concat_rows(const int32_t *row_ids, int64_t n_tokens,
+                                            int32_t n_heads, const engram_tables *tables_host,
+                                            uint16_t *e_out, uint8_t *state_out, int32_t *status,
+                                            void *stream) {
+  const char *fn = "engram_concat_rows";
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
+  engram_status st = check_connection_tables(fn, n_heads, tables_host);
+  if (st != ENGRAM_OK) return st;
+  if (n_tokens == 0) return ok();
+  if (!row_ids || !e_out || !state_out || !aligned(row_ids, 4) || !aligned(e_out, 16) ||
+      !aligned(status, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: NULL or misaligned buffer", fn);
+  if ((st = check_device()) != ENGRAM_OK) return st;
+  return launched("engram_concat_rows launch",
+                  engram::launch_concat_rows(row_ids, n_tokens, n_heads, *tables_host, e_out,
+                                             state_out, status, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_wkv_project(const uint16_t *e, int64_t n_tokens, int32_t K,
+                                            const uint16_t *wkv, int32_t D, float *k_out,
+                                            int32_t *status, void *stream) {
+  const char *fn = "engram_wkv_project";
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
+  engram_status st = check_projection(fn, K, D);
+  if (st != ENGRAM_OK) return st;
+  if (!wkv || !aligned(wkv, 16))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: wkv NULL or not 16-byte aligned", fn);
+  if (n_tokens == 0) return ok();
+  if (!e || !k_out || !aligned(e, 16) || !aligned(k_out, 16) || !aligned(status, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: NULL or misaligned buffer", fn);
+  if ((st = check_device()) != ENGRAM_OK) return st;
+  return launched("engram_wkv_project launch",
+                  engram::launch_wkv_gemm(e, wkv, k_out, (int)n_tokens, D, K,
+                                          g_wait_limit_ns.load(std::memory_order_relaxed), status,
+                                          (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, int64_t n_tokens,
+                                         int32_t D, const uint16_t *streams_in,
+                                         uint16_t *streams_out, const float *alpha, float eps,
+                                         float *gate_out, void *stream) {
+  const char *fn = "engram_gate_add";
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
+  if (D < 16 || D % 16 != 0 || D > 8192)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: D must be a multiple of 16 in [16, 8192]", fn);
+  engram_status st = check_gate_add(fn, n_tokens, D, streams_in, streams_out, alpha, eps, gate_out);
+  if (st != ENGRAM_OK) return st;
+  if (n_tokens == 0) return ok();
+  if (!k || !state || !aligned(k, 16))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: k or state NULL, or k misaligned", fn);
+  if ((st = check_device()) != ENGRAM_OK) return st;
+  return launched("engram_gate_add launch",
+                  engram::launch_gate_add(k, state, n_tokens, D, streams_in, streams_out, alpha,
+                                          eps, gate_out, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_connection(const int32_t *row_ids, int64_t n_tokens,
+                                           int32_t n_heads, const engram_tables *tables_host,
+                                           const uint16_t *wkv, int32_t D,
+                                           const uint16_t *streams_in, uint16_t *streams_out,
+                                           const float *alpha, float eps, void *workspace,
+                                           size_t workspace_bytes, float *gate_out, float *k_out,
+                                           int32_t *status, void *stream) {
+  const char *fn = "engram_connection";
+  if (n_tokens < 0 || n_tokens > INT32_MAX)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
+  engram_status st = check_connection_tables(fn, n_heads, tables_host);
+  if (st != ENGRAM_OK) return st;
+  const int d = tables_host->D;
+  const int64_t K = 3 * (int64_t)n_heads * d;
+  if ((st = check_projection(fn, K, D)) != ENGRAM_OK) return st;
+  if (!wkv || !aligned(wkv, 16))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: wkv NULL or not 16-byte aligned", fn);
+  st = check_gate_add(fn, n_tokens, D, streams_in, streams_out, alpha, eps, gate_out);
+  if (st != ENGRAM_OK) return st;
+  if (n_tokens == 0) return ok();
+  const size_t need = engram_connection_workspace_bytes(n_tokens, n_heads, d, D);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(ENGRAM_ERR_INVALID_ARG,
+                "%s: workspace NULL, not 256-byte aligned or under %zu bytes", fn, need);
+  if (!row_ids || !aligned(row_ids, 4) || !aligned(k_out, 16) || !aligned(status, 4))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: NULL or misaligned buffer", fn);
+  if ((st = check_device()) != ENGRAM_OK) return st;
+  char *w = static_cast<char *>(workspace);
+  uint16_t *e = reinterpret_cast<uint16_t *>(w);
+  w += round256((size_t)n_tokens * K * 2);
+  float *k = k_out ? k_out : reinterpret_cast<float *>(w);
+  w += round256((size_t)n_tokens * D * 4);
+  uint8_t *state = reinterpret_cast<uint8_t *>(w);
+  return launched("engram_connection launch",
+                  engram::launch_connection(row_ids, n_tokens, n_heads, *tables_host, wkv, D,
+                                            streams_in, streams_out, alpha, eps, e, k, state,
+                                            gate_out, g_wait_limit_ns.load(std::memory_order_relaxed),
+                                            status, (cudaStream_t)stream));
+}
+
 ENGRAM_API int32_t engram_set_lookup_kernel(int32_t which) {
   if (which != ENGRAM_LOOKUP_AUTO && which != ENGRAM_LOOKUP_GATHER && which != ENGRAM_LOOKUP_BULK)
     return -1;

@@ -69,6 +69,20 @@ cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream)
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_supported(int D, int dtype, int H);
 
+bool wkv_gemm_supported(int N, int K);
+cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out, int T, int N, int K,
+                            int64_t wait_limit_ns, int32_t *status, cudaStream_t stream);
+cudaError_t launch_concat_rows(const int32_t *row_ids, int64_t T, int H, const engram_tables &tb,
+                               uint16_t *e, uint8_t *state, int32_t *status, cudaStream_t stream);
+cudaError_t launch_gate_add(const float *k, const uint8_t *state, int64_t T, int D,
+                            const uint16_t *x, uint16_t *y, const float *alpha, float eps,
+                            float *gate_out, cudaStream_t stream);
+cudaError_t launch_connection(const int32_t *row_ids, int64_t T, int H, const engram_tables &tb,
+                              const uint16_t *wkv, int D, const uint16_t *x, uint16_t *y,
+                              const float *alpha, float eps, uint16_t *e, float *k,
+                              uint8_t *state, float *gate_out, int64_t wait_limit_ns,
+                              int32_t *status, cudaStream_t stream);
+
 // Records the message engram_last_error() returns on this thread; returns code.
 engram_status set_error(engram_status code, const char *fmt, ...);
 

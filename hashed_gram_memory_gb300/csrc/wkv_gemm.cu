@@ -1,0 +1,307 @@
+// wkv_gemm.cu -- k = E wkv^T on the sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// E [T, K] bf16 (the tokens' concatenated rows) times wkv [N, K] bf16 (one row of
+// weights per output) gives k [T, N] fp32.  One CTA computes a 128 x 256 tile of
+// k: a 4-stage ring of shared-memory stages, each holding a 128 x 64 slice of E
+// and a 256 x 64 slice of wkv (one 128-byte swizzle atom along K), filled by
+// 2-D TMA loads that complete on the stage's mbarrier.  One thread issues the
+// tcgen05.mma instructions (M = 128, N = 256, K = 16, bf16 in, fp32 accumulated
+// in 256 TMEM columns) and commits each stage back to the producer through an
+// mbarrier when its MMAs have read it; a final commit hands the accumulator to
+// the four warps, which read it with tcgen05.ld (warp w owns TMEM lanes 32w..)
+// and store fp32 rows.
+//
+// Every mbarrier wait is bounded (SM clock cycles): a wait that gives up sets
+// ENGRAM_FLAG_TIMEOUT and a shared abort flag, after which no warp issues more
+// work, the tile is not stored, the issued copies and MMAs are waited for
+// (bounded), and the TMEM columns are freed before the block exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "engram_internal.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 256;          // fp32 accumulator, one column per output
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + 256;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the phase of `bar` with parity `parity`, giving up after about
+// limit_ns (SM cycles at 2.1 GHz, checked every 32 polls) or as soon as another
+// thread raised the abort flag.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           int64_t limit_ns, int32_t *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long limit = limit_ns * 21 / 10;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        if (status) atomicOr(status, ENGRAM_FLAG_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (draining work already issued).
+__device__ __forceinline__ void drain_phase(uint64_t *bar, uint32_t parity, int64_t limit_ns) {
+  const long long limit = limit_ns * 21 / 10;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > limit) return;
+}
+
+// 2-D TMA tile load (coordinates: x = K offset, y = row) completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the
+// 128-byte swizzle (rows of 128 bytes, 8-row atoms 1024 bytes apart): start
+// address, stride between 8-row groups 1024 B, descriptor version 1, layout
+// SWIZZLE_128B (2).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)2 << 61;                  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 256, M = 128.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                                ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a_desc), "l"(b_desc), "r"(kInstrDesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(128, 1)
+    wkv_gemm_kernel(const __grid_constant__ CUtensorMap map_e, const __grid_constant__ CUtensorMap map_w,
+                    float *__restrict__ k_out, int T, int N, int K, int64_t wait_limit_ns,
+                    int32_t *status) {
+  extern __shared__ uint8_t sm_raw[];
+  // 1024-byte alignment for the swizzled tiles.
+  uint8_t *sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
+  uint8_t *stage_base = sm;
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + kStages * kStageBytes);
+  uint64_t *empty = full + kStages;
+  uint64_t *accum = empty + kStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+  const int kblocks = K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {  // the whole warp allocates the accumulator's TMEM columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------- TMA producer
+    int issued = 0;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1;
+      if (!wait_phase(empty + s, ph ^ 1, abort_flag, wait_limit_ns, status)) break;
+      uint8_t *a = stage_base + s * kStageBytes;
+      mbar_arrive_expect_tx(full + s, kStageBytes);
+      tma_load_2d(a, &map_e, kb * kBK, m0, full + s);
+      tma_load_2d(a + kABytes, &map_w, kb * kBK, n0, full + s);
+      ++issued;
+    }
+    // Loads issued into shared memory land before the block can exit.
+    for (int kb = issued - kStages > 0 ? issued - kStages : 0; kb < issued; ++kb)
+      drain_phase(full + kb % kStages, (kb / kStages) & 1, wait_limit_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    for (int kb = 0; kb < kblocks; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1;
+      if (!wait_phase(full + s, ph, abort_flag, wait_limit_ns, status)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t a = smem_u32(stage_base + s * kStageBytes);
+      const uint32_t b = a + kABytes;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k)  // advance 16 bf16 = 32 bytes along K per MMA
+        umma_bf16(tmem, smem_desc_sw128(a + 32 * k), smem_desc_sw128(b + 32 * k),
+                  (kb | k) != 0 ? 1u : 0u);
+      umma_commit(empty + s);  // the stage is free once these MMAs have read it
+    }
+    umma_commit(accum);  // arrives when every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- epilogue
+  const bool ok = wait_phase(accum, 0, abort_flag, wait_limit_ns, status);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const bool store = __syncthreads_and(ok && *abort_flag == 0);
+  const int row = m0 + warp * 32 + lane;
+  if (store) {
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      uint32_t v[32];
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+          "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+          "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+            "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+            "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+            "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+            "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+            "=r"(v[31])
+          : "r"(taddr)
+          : "memory");
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (row < T) {
+        float4 *dst = reinterpret_cast<float4 *>(k_out + (int64_t)row * N + n0 + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    // Aborted: wait (bounded) for the MMAs already issued before freeing TMEM.
+    drain_phase(accum, 0, wait_limit_ns);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                 const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                 const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  }
+  return fn;
+}
+
+// A row-major bf16 matrix [rows, cols] (cols contiguous) as a 2-D tiled map with
+// box [64 cols, box_rows], 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool wkv_gemm_supported(int N, int K) { return N % kBN == 0 && K % kBK == 0 && K > 0 && N > 0; }
+
+cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out, int T, int N, int K,
+                            int64_t wait_limit_ns, int32_t *status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  CUtensorMap map_e, map_w;
+  if (!make_map(&map_e, e, (uint64_t)T, (uint64_t)K, kBM) ||
+      !make_map(&map_w, wkv, (uint64_t)N, (uint64_t)K, kBN))
+    return cudaErrorInvalidValue;
+  cudaError_t err =
+      cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid((T + kBM - 1) / kBM, N / kBN);
+  wkv_gemm_kernel<<<grid, 128, kSmemBytes, stream>>>(map_e, map_w, k_out, T, N, K, wait_limit_ns,
+                                                     status);
+  return cudaGetLastError();
+}
+
+}  // namespace engram

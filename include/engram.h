@@ -245,6 +245,79 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
                                              float *mem_out, int32_t *status, void *stream);
 
 /*
+ * engram_connection -- the Engram connection with a wkv projection in place of
+ * the mean: the other half of Engram, "wkv and the gate", which reads the mHC
+ * streams (VeOmni PR page, "n-gram memory lookup" commit and the DeepSeek-V4.1
+ * layer commit; the gathered rows cross to it as n-gram embeddings, about 24 KB
+ * a token = 3 orders x 8 heads x 256 columns x 2 layers x 2 bytes).  The pages give
+ * no formula; this library reads it as, per token with K = 3*n_heads*d:
+ *   e     = the 3*n_heads dequantised rows concatenated in (order, head) order,
+ *           K values, each exact in bf16 (BF16 tables, or FP8 e4m3fn with
+ *           (1, 32) e8m0 block exponents)
+ *   k     = wkv e, fp32 accumulation on the tensor cores (wkv bf16 [D, K],
+ *           row j = output j's weights)
+ *   g     = sigmoid(<rmsnorm(stream0), rmsnorm(k)> / sqrt(D)), as above with k
+ *           in place of m
+ *   out_s = bf16_rne(stream_s + g * alpha_s * k)
+ * Three launches on `stream`: the rows into E (bf16 [n_tokens, K], workspace),
+ * k = E wkv^T (tcgen05 tensor cores, TMA, fp32 in tensor memory), then the gate
+ * and the add.
+ *   row_ids      int32 [n_tokens, 3*n_heads], as for engram_lookup_fused
+ *   tables_host  dtype ENGRAM_TABLE_BF16 or ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;
+ *                D (the row width d) a multiple of 32
+ *   wkv          bf16 bits [D, K], 16-byte aligned; D a multiple of 256 in
+ *                [256, 8192] and K a multiple of 64
+ *   streams_in / streams_out / alpha / eps / gate_out as engram_lookup_fused
+ *   workspace    device, 256-byte aligned, at least
+ *                engram_connection_workspace_bytes(n_tokens, n_heads, d, D)
+ *                bytes, owned by the caller, busy until the call's kernels end
+ *   k_out        fp32 [n_tokens, D] or NULL (16-byte aligned): k per token (0
+ *                for a dead or bad token); NULL keeps k in the workspace
+ * Dead tokens and bad rows as engram_lookup_fused.  A projection that does not
+ * complete within the wait limit sets ENGRAM_FLAG_TIMEOUT and leaves k
+ * unwritten for its tile.  Other table types give ENGRAM_ERR_UNSUPPORTED.
+ */
+ENGRAM_API size_t engram_connection_workspace_bytes(int64_t n_tokens, int32_t n_heads, int32_t d,
+                                                    int32_t D);
+ENGRAM_API engram_status engram_connection(const int32_t *row_ids, int64_t n_tokens,
+                                           int32_t n_heads, const engram_tables *tables_host,
+                                           const uint16_t *wkv, int32_t D,
+                                           const uint16_t *streams_in, uint16_t *streams_out,
+                                           const float *alpha, float eps, void *workspace,
+                                           size_t workspace_bytes, float *gate_out, float *k_out,
+                                           int32_t *status, void *stream);
+
+/*
+ * The three stages of engram_connection as calls of their own (the same kernels,
+ * for callers that keep E or k, and for timing the projection alone):
+ *
+ * engram_concat_rows -- E[t] = the token's 3*n_heads dequantised rows in (order,
+ *   head) order, bf16 bits [n_tokens, K], K = 3*n_heads*d (e_out 16-byte
+ *   aligned), and state_out uint8 [n_tokens]: 0 live, 1 dead (every id
+ *   ENGRAM_ROW_DEAD; E[t] = 0), 2 bad row (ENGRAM_FLAG_BAD_ROW raised; E[t] = 0).
+ *   Tables as for engram_connection.
+ * engram_wkv_project -- k = E wkv^T: e bf16 bits [n_tokens, K], wkv bf16 bits [D,
+ *   K], k_out fp32 [n_tokens, D]; all 16-byte aligned; D a multiple of 256 in
+ *   [256, 8192], K a multiple of 64.  tcgen05 tensor cores, fp32 accumulation.
+ * engram_gate_add -- per token with state 0: g = sigmoid(<rmsnorm(stream0),
+ *   rmsnorm(k)> / sqrt(D)), out_s = bf16_rne(stream_s + g * alpha_s * k); state
+ *   1: streams copied through, g = 0; state 2: nothing written.  k fp32 [n_tokens,
+ *   D] (16-byte aligned), D a multiple of 16 in [16, 8192]; streams, alpha, eps
+ *   and gate_out as engram_lookup_fused.
+ */
+ENGRAM_API engram_status engram_concat_rows(const int32_t *row_ids, int64_t n_tokens,
+                                            int32_t n_heads, const engram_tables *tables_host,
+                                            uint16_t *e_out, uint8_t *state_out, int32_t *status,
+                                            void *stream);
+ENGRAM_API engram_status engram_wkv_project(const uint16_t *e, int64_t n_tokens, int32_t K,
+                                            const uint16_t *wkv, int32_t D, float *k_out,
+                                            int32_t *status, void *stream);
+ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, int64_t n_tokens,
+                                         int32_t D, const uint16_t *streams_in,
+                                         uint16_t *streams_out, const float *alpha, float eps,
+                                         float *gate_out, void *stream);
+
+/*
  * engram_forward -- the whole path in one call on device buffers:
  * engram_compress, engram_hash and engram_lookup_fused back to back on
  * `stream`, with the compressed ids and row ids kept in `workspace` (device
@@ -368,7 +441,7 @@ ENGRAM_API const char *engram_status_string(engram_status code);
 ENGRAM_API const char *engram_last_error(void);
 
 /* ABI version of this header (incremented on any incompatible change). */
-#define ENGRAM_ABI_VERSION 2
+#define ENGRAM_ABI_VERSION 3
 ENGRAM_API int32_t engram_abi_version(void);
 
 #ifdef __cplusplus

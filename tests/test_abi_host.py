@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol(eg):
 
 
 def test_abi_version_and_strings(eg):
-    assert eg.engram_abi_version() == 2
+    assert eg.engram_abi_version() == 3
     for code in range(6):
         assert eg.engram_status_string(code).startswith("ENGRAM")
     assert "unknown" in eg.engram_status_string(99)
@@ -121,6 +121,53 @@ def test_host_argument_errors(eg):
     tb = _tables(dtype=1, scale=0)
     assert L.engram_lookup_fused(ids, 0, 2, C.byref(tb), None, None, a, 1e-6, None, None, None,
                                  None) == eg.OK
+
+
+def test_connection_host_argument_errors(eg):
+    """engram_connection and its three stages check their arguments on the host,
+    before any device query or launch."""
+    L = eg.lib
+    INV, UNS, OK = eg.ERR_INVALID_ARG, eg.ERR_UNSUPPORTED, eg.OK
+    ids, w, x, y, a = (C.c_void_p(v) for v in (0x4000, 0x8000000, 0x100000000, 0x200000000, 0x3000))
+    ws = C.c_void_p(0x300000000)
+    e8 = _tables(dtype=2, D=256)
+    need = eg.engram_connection_workspace_bytes(100, 8, 256, 4096)
+    assert need == 100 * 6144 * 2 + 100 * 4096 * 4 + 256   # E, k, state (256-byte rounded)
+
+    def conn(tb, D=4096, H=8, n=100, wkv=w, xin=x, out=y, alpha=a, eps=1e-6, work=ws, wb=need):
+        return L.engram_connection(ids, n, H, C.byref(tb) if tb is not None else None, wkv, D,
+                                   xin, out, alpha, eps, work, wb, None, None, None, None)
+
+    assert conn(_tables(dtype=0, D=256)) == UNS            # per-row fp32 scales: not exact in bf16
+    assert conn(e8, D=4000) == UNS                         # D not a multiple of 256
+    assert conn(e8, D=8448) == UNS                         # D above 8192
+    assert conn(_tables(dtype=2, D=48)) == INV             # row width not a multiple of 32
+    assert conn(_tables(dtype=1, D=32, scale=0), H=1, n=5) == UNS  # K = 96 not a multiple of 64
+    assert conn(None) == INV
+    assert conn(e8, H=0) == INV
+    assert conn(_tables(dtype=2, D=256, scale=0)) == INV   # e8m0 tables need their exponents
+    assert conn(e8, wkv=C.c_void_p(0x8000008)) == INV      # wkv not 16-byte aligned
+    assert conn(e8, alpha=None) == INV
+    assert conn(e8, eps=float("nan")) == INV
+    assert conn(e8, wb=need - 1) == INV                    # short workspace
+    assert conn(e8, work=C.c_void_p(0x300000080)) == INV   # workspace not 256-byte aligned
+    assert conn(e8, out=C.c_void_p(0x100000010)) == INV    # partial overlap of the streams
+    assert conn(e8, n=0, work=None, wb=0) == OK            # nothing to do
+
+    e, k, st = C.c_void_p(0x500000000), C.c_void_p(0x600000000), C.c_void_p(0x7000)
+    assert L.engram_concat_rows(ids, 10, 8, C.byref(_tables(dtype=0, D=256)), e, st, None,
+                                None) == UNS
+    assert L.engram_concat_rows(ids, 10, 8, C.byref(e8), C.c_void_p(0x500000008), st, None,
+                                None) == INV
+    assert L.engram_concat_rows(ids, 0, 8, C.byref(e8), None, None, None, None) == OK
+    assert L.engram_wkv_project(e, 10, 6144, w, 300, k, None, None) == UNS
+    assert L.engram_wkv_project(e, 10, 6100, w, 4096, k, None, None) == UNS
+    assert L.engram_wkv_project(e, 10, 6144, w, 4096, C.c_void_p(0x600000004), None, None) == INV
+    assert L.engram_wkv_project(None, 0, 6144, w, 4096, None, None, None) == OK
+    assert L.engram_gate_add(k, st, 10, 4095, x, y, a, 1e-6, None, None) == INV
+    assert L.engram_gate_add(k, st, 10, 8208, x, y, a, 1e-6, None, None) == INV
+    assert L.engram_gate_add(k, None, 10, 4096, x, y, a, 1e-6, None, None) == INV
+    assert L.engram_gate_add(None, None, 0, 4096, None, None, a, 1e-6, None, None) == OK
 
 
 def test_python_binding_rejects_cpu_tensors(eg):

@@ -27,7 +27,8 @@ import dataclasses
 import numpy as np
 
 # Input kinds: one independent PCG64 stream per kind.
-_K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS, _K_PACK = range(9)
+_K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS, _K_PACK, _K_WKV = \
+    range(10)
 
 FP8 = "fp8_e4m3fn"
 BF16 = "bf16"
@@ -67,6 +68,12 @@ class EngramConfig:
     # above hash_vocab (0: one table per n-gram order)
     hash_vocab: int = 0
     eps: float = 1e-6
+    # The connection with a wkv projection: the 3H rows (width D) concatenated and
+    # projected to `hidden` columns by wkv bf16 [hidden, 3H*D] from N(0, wkv_std^2);
+    # the streams are then [B, S, 4, hidden].  0: no projection (the mean; streams
+    # have the row width D)
+    hidden: int = 0
+    wkv_std: float = 1.0
 
     @property
     def T(self) -> int:
@@ -75,6 +82,16 @@ class EngramConfig:
     @property
     def R(self) -> int:
         return 3 * self.H
+
+    @property
+    def width(self) -> int:
+        """Width of the mHC streams: hidden with a projection, else the row width."""
+        return self.hidden or self.D
+
+    @property
+    def K(self) -> int:
+        """Width of a token's concatenated rows (the projection's inner dimension)."""
+        return self.R * self.D
 
     def scaled(self, **kw) -> "EngramConfig":
         """Same distributions, other sizes (for parity cases the oracle finishes quickly)."""
@@ -98,7 +115,11 @@ class EngramConfig:
         """Bytes the fused lookup must move per token, with no cache credit:
         3H rows (+ their scales), the 3H int32 row ids, and the four bf16 streams
         read once and written once."""
-        return self.R * self.row_bytes() + self.R * 4 + 2 * 4 * self.D * 2
+        return self.R * self.row_bytes() + self.R * 4 + 2 * 4 * self.width * 2
+
+    def connection_flops_per_token(self) -> int:
+        """Multiply-adds of k = wkv e, counted as 2 flops each."""
+        return 2 * self.hidden * self.K
 
 
 CONFIGS = [
@@ -133,6 +154,12 @@ CONFIGS = [
     EngramConfig(name="release_layout_fp8", seed=7, B=8, S=8192, vocab=129_280, n_eids=100_000,
                  H=8, D=256, rows=(384_006_168,) * 3, dtype=FP8_E8M0, ids="zipf",
                  repeat_frac=0.05, hash_vocab=16_000_000),
+    # 8: the connection with a wkv projection on the released table layout: a
+    #    token's 24 rows of 256 (K = 6144) projected to the 4096-wide streams;
+    #    wkv_std 2 gives k about the streams' unit scale (rows ~ 0.0045 rms)
+    EngramConfig(name="release_connection_e8m0", seed=8, B=8, S=8192, vocab=129_280,
+                 n_eids=100_000, H=8, D=256, rows=(384_006_168,) * 3, dtype=FP8_E8M0, ids="zipf",
+                 repeat_frac=0.05, hash_vocab=16_000_000, hidden=4096, wkv_std=2.0),
 ]
 
 
@@ -244,9 +271,16 @@ def _to_e4m3_bytes(x: np.ndarray) -> np.ndarray:
 
 
 def streams_host(cfg: EngramConfig, rank: int = 0) -> np.ndarray:
-    """[B, S, 4, D] bf16 bit patterns (uint16), N(0,1)."""
+    """[B, S, 4, width] bf16 bit patterns (uint16), N(0,1)."""
     g = rng(cfg, _K_STREAMS, rank)
-    x = g.standard_normal((cfg.B, cfg.S, 4, cfg.D), dtype=np.float32)
+    x = g.standard_normal((cfg.B, cfg.S, 4, cfg.width), dtype=np.float32)
+    return _to_bf16_bits(x)
+
+
+def wkv_host(cfg: EngramConfig) -> np.ndarray:
+    """[hidden, K] bf16 bit patterns (uint16), N(0, wkv_std^2)."""
+    g = rng(cfg, _K_WKV)
+    x = g.standard_normal((cfg.hidden, cfg.K), dtype=np.float32) * np.float32(cfg.wkv_std)
     return _to_bf16_bits(x)
 
 
@@ -326,16 +360,24 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
 
 
 def streams_device(cfg: EngramConfig, device, rank: int = 0, chunk_tokens: int = 4096):
-    """[B, S, 4, D] bf16 N(0,1) streams generated on the GPU (as int16 bits)."""
+    """[B, S, 4, width] bf16 N(0,1) streams generated on the GPU (as int16 bits)."""
     import torch
-    out = torch.empty((cfg.T, 4, cfg.D), dtype=torch.int16, device=device)
+    out = torch.empty((cfg.T, 4, cfg.width), dtype=torch.int16, device=device)
     g = _dev_gen(device, cfg.seed * 1_000_003 + 977 + 13 * rank)
     for t0 in range(0, cfg.T, chunk_tokens):
         t1 = min(cfg.T, t0 + chunk_tokens)
-        x = torch.randn((t1 - t0, 4, cfg.D), generator=g, device=device, dtype=torch.float32)
+        x = torch.randn((t1 - t0, 4, cfg.width), generator=g, device=device, dtype=torch.float32)
         out[t0:t1] = x.to(torch.bfloat16).view(torch.int16)
         del x
-    return out.view(cfg.B, cfg.S, 4, cfg.D)
+    return out.view(cfg.B, cfg.S, 4, cfg.width)
+
+
+def wkv_device(cfg: EngramConfig, device):
+    """[hidden, K] bf16 N(0, wkv_std^2) projection generated on the GPU (as int16 bits)."""
+    import torch
+    g = _dev_gen(device, cfg.seed * 1_000_003 + 4099)
+    x = torch.randn((cfg.hidden, cfg.K), generator=g, device=device, dtype=torch.float32)
+    return x.mul_(cfg.wkv_std).to(torch.bfloat16).view(torch.int16)
 
 
 def bytes_human(n: float) -> str:
