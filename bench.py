@@ -54,6 +54,9 @@ def parse():
                     help="override the batch (small cases for ncu captures)")
     ap.add_argument("--rows", type=int, default=0,
                     help="override the rows of each table (small cases for ncu captures)")
+    ap.add_argument("--hash-vocab", type=int, default=0,
+                    help="override the bucketed layout's hash vocabulary (the table shrinks to "
+                         "the sum of its buckets; small cases for ncu captures)")
     ap.add_argument("--lookup-kernel", default="auto", choices=["auto", "gather", "bulk"])
     return ap.parse_args()
 
@@ -64,6 +67,10 @@ def config_of(name: str, args=None) -> W.EngramConfig:
         cfg = cfg.scaled(B=args.batch)
     if args is not None and args.rows:
         cfg = cfg.scaled(rows=(args.rows,) * 3)
+    if args is not None and args.hash_vocab and cfg.hash_vocab:
+        import hashed_gram_memory_gb300 as eg
+        total = sum(sum(o) for o in eg.engram_bucket_primes(1, 4, cfg.H, args.hash_vocab)[0])
+        cfg = cfg.scaled(hash_vocab=args.hash_vocab, rows=(total,) * 3)
     return cfg
 
 

@@ -134,8 +134,8 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 
 __global__ void __launch_bounds__(128, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap map_e, const __grid_constant__ CUtensorMap map_w,
-                    float *__restrict__ k_out, int T, int N, int K, int64_t wait_limit_ns,
-                    int32_t *status) {
+                    float *__restrict__ k_out, int T, int N, int K, int m_tile0,
+                    int64_t wait_limit_ns, int32_t *status) {
   extern __shared__ uint8_t sm_raw[];
   // 1024-byte alignment for the swizzled tiles.
   uint8_t *sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
@@ -147,7 +147,9 @@ __global__ void __launch_bounds__(128, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+  // N tiles vary fastest: the CTAs resident at one time share a few M tiles of E
+  // (read from HBM once) and sweep all of wkv (L2-resident).
+  const int m0 = (m_tile0 + blockIdx.y) * kBM, n0 = blockIdx.x * kBN;
   const int kblocks = K / kBK;
 
   if (threadIdx.x == 0) {
@@ -298,10 +300,15 @@ cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out
   cudaError_t err =
       cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  dim3 grid((T + kBM - 1) / kBM, N / kBN);
-  wkv_gemm_kernel<<<grid, 128, kSmemBytes, stream>>>(map_e, map_w, k_out, T, N, K, wait_limit_ns,
-                                                     status);
-  return cudaGetLastError();
+  const int m_tiles = (T + kBM - 1) / kBM;
+  for (int m_tile0 = 0; m_tile0 < m_tiles; m_tile0 += 65535) {  // gridDim.y limit
+    const dim3 grid(N / kBN, m_tiles - m_tile0 < 65535 ? m_tiles - m_tile0 : 65535);
+    wkv_gemm_kernel<<<grid, 128, kSmemBytes, stream>>>(map_e, map_w, k_out, T, N, K, m_tile0,
+                                                       wait_limit_ns, status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace engram
