@@ -1,20 +1,28 @@
 // wkv_gemm.cu -- k = E wkv^T on the sm_103a tensor cores (tcgen05 + TMA + TMEM).
 //
 // E [T, K] bf16 (the tokens' concatenated rows) times wkv [N, K] bf16 (one row of
-// weights per output) gives k [T, N] fp32.  One CTA computes a 128 x 256 tile of
-// k: a 4-stage ring of shared-memory stages, each holding a 128 x 64 slice of E
-// and a 256 x 64 slice of wkv (one 128-byte swizzle atom along K), filled by
-// 2-D TMA loads that complete on the stage's mbarrier.  One thread issues the
-// tcgen05.mma instructions (M = 128, N = 256, K = 16, bf16 in, fp32 accumulated
-// in 256 TMEM columns) and commits each stage back to the producer through an
-// mbarrier when its MMAs have read it; a final commit hands the accumulator to
-// the four warps, which read it with tcgen05.ld (warp w owns TMEM lanes 32w..)
-// and store fp32 rows.
+// weights per output) gives k [T, N] fp32, in 128 x 256 tiles of k.  A persistent
+// kernel, one CTA per SM, walks the tiles in order (N tiles fastest, so the CTAs
+// resident at one time share a few 128-row slices of E, read from HBM once, and
+// sweep wkv, which stays in L2).  Six warps per CTA:
+//   warp 0, one thread : TMA producer -- fills a 4-stage shared-memory ring, each
+//                        stage a 128 x 64 slice of E and a 256 x 64 slice of wkv
+//                        (one 128-byte swizzle atom along K), completing on the
+//                        stage's mbarrier;
+//   warp 1             : allocates the 512 TMEM columns; one thread issues the
+//                        tcgen05.mma instructions (M 128, N 256, K 16, bf16 in,
+//                        fp32 accumulated) into one of two 256-column
+//                        accumulators, frees each stage through an mbarrier once
+//                        its MMAs have read it, and hands a finished accumulator
+//                        to the epilogue through another;
+//   warps 2..5         : the epilogue -- each reads its 32 TMEM lanes (tcgen05.ld)
+//                        and stores fp32 rows of k, then returns the accumulator,
+//                        so a tile's epilogue runs under the next tile's MMAs.
 //
 // Every mbarrier wait is bounded (SM clock cycles): a wait that gives up sets
 // ENGRAM_FLAG_TIMEOUT and a shared abort flag, after which no warp issues more
-// work, the tile is not stored, the issued copies and MMAs are waited for
-// (bounded), and the TMEM columns are freed before the block exits.
+// work and the tiles not yet stored stay unwritten; the issued copies and MMAs
+// are waited for (bounded) and the TMEM columns freed before the block exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -24,10 +32,12 @@ namespace engram {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kThreads = 192;                // producer, MMA, four epilogue warps
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = 256;          // fp32 accumulator, one column per output
+constexpr uint32_t kAccCols = 256;           // one fp32 accumulator: a column per output
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // two accumulators: all 512 columns
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes + 256;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -42,6 +52,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -132,36 +146,41 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
       : "memory");
 }
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap map_e, const __grid_constant__ CUtensorMap map_w,
-                    float *__restrict__ k_out, int T, int N, int K, int m_tile0,
-                    int64_t wait_limit_ns, int32_t *status) {
+                    float *__restrict__ k_out, int T, int N, int K, int64_t wait_limit_ns,
+                    int32_t *status) {
   extern __shared__ uint8_t sm_raw[];
   // 1024-byte alignment for the swizzled tiles.
   uint8_t *sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
   uint8_t *stage_base = sm;
   uint64_t *full = reinterpret_cast<uint64_t *>(sm + kStages * kStageBytes);
   uint64_t *empty = full + kStages;
-  uint64_t *accum = empty + kStages;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+  uint64_t *acc_full = empty + kStages;  // [2] MMA -> epilogue
+  uint64_t *acc_empty = acc_full + 2;    // [2] epilogue -> MMA (one arrive per epilogue warp)
+  uint64_t *mma_done = acc_empty + 2;    // every MMA issued has completed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // N tiles vary fastest: the CTAs resident at one time share a few M tiles of E
-  // (read from HBM once) and sweep all of wkv (L2-resident).
-  const int m0 = (m_tile0 + blockIdx.y) * kBM, n0 = blockIdx.x * kBN;
   const int kblocks = K / kBK;
+  const int n_tiles_n = N / kBN;
+  const int64_t n_tiles = (int64_t)((T + kBM - 1) / kBM) * n_tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    mbar_init(accum, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full + a, 1);
+      mbar_init(acc_empty + a, 4);
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {  // the whole warp allocates the accumulator's TMEM columns
+  if (warp == 1) {  // the whole warp allocates the accumulators' TMEM columns
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -173,79 +192,105 @@ __global__ void __launch_bounds__(128, 1)
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------- TMA producer
-    int issued = 0;
-    for (int kb = 0; kb < kblocks; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1;
-      if (!wait_phase(empty + s, ph ^ 1, abort_flag, wait_limit_ns, status)) break;
-      uint8_t *a = stage_base + s * kStageBytes;
-      mbar_arrive_expect_tx(full + s, kStageBytes);
-      tma_load_2d(a, &map_e, kb * kBK, m0, full + s);
-      tma_load_2d(a + kABytes, &map_w, kb * kBK, n0, full + s);
-      ++issued;
-    }
-    // Loads issued into shared memory land before the block can exit.
-    for (int kb = issued - kStages > 0 ? issued - kStages : 0; kb < issued; ++kb)
-      drain_phase(full + kb % kStages, (kb / kStages) & 1, wait_limit_ns);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    for (int kb = 0; kb < kblocks; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1;
-      if (!wait_phase(full + s, ph, abort_flag, wait_limit_ns, status)) break;
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t a = smem_u32(stage_base + s * kStageBytes);
-      const uint32_t b = a + kABytes;
-#pragma unroll
-      for (int k = 0; k < kBK / 16; ++k)  // advance 16 bf16 = 32 bytes along K per MMA
-        umma_bf16(tmem, smem_desc_sw128(a + 32 * k), smem_desc_sw128(b + 32 * k),
-                  (kb | k) != 0 ? 1u : 0u);
-      umma_commit(empty + s);  // the stage is free once these MMAs have read it
-    }
-    umma_commit(accum);  // arrives when every MMA issued above has completed
-  }
-  __syncwarp();
-
-  // ---------------------------------------------------------------- epilogue
-  const bool ok = wait_phase(accum, 0, abort_flag, wait_limit_ns, status);
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const bool store = __syncthreads_and(ok && *abort_flag == 0);
-  const int row = m0 + warp * 32 + lane;
-  if (store) {
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      uint32_t v[32];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32);
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-          "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-          "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-            "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-            "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-            "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-            "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-            "=r"(v[31])
-          : "r"(taddr)
-          : "memory");
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (row < T) {
-        float4 *dst = reinterpret_cast<float4 *>(k_out + (int64_t)row * N + n0 + c * 32);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+  if (warp == 0) {
+    if (lane == 0) {
+      // -------------------------------------------------------- TMA producer
+      uint32_t it = 0;  // k-blocks issued, over all of this CTA's tiles
+      for (int64_t tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+        const int m0 = (int)(tile / n_tiles_n) * kBM, n0 = (int)(tile % n_tiles_n) * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!(ok = wait_phase(empty + s, ph ^ 1, abort_flag, wait_limit_ns, status))) break;
+          uint8_t *a = stage_base + s * kStageBytes;
+          mbar_arrive_expect_tx(full + s, kStageBytes);
+          tma_load_2d(a, &map_e, kb * kBK, m0, full + s);
+          tma_load_2d(a + kABytes, &map_w, kb * kBK, n0, full + s);
+        }
+        if (!ok) break;
       }
+      // Loads issued into shared memory land before the block can exit.
+      for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
+        drain_phase(full + j % kStages, (j / kStages) & 1, wait_limit_ns);
     }
-  } else if (threadIdx.x == 0) {
-    // Aborted: wait (bounded) for the MMAs already issued before freeing TMEM.
-    drain_phase(accum, 0, wait_limit_ns);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t it = 0, local = 0;
+      for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+        const uint32_t acc = local & 1, use = local >> 1;
+        if (!wait_phase(acc_empty + acc, (use & 1) ^ 1, abort_flag, wait_limit_ns, status)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d_tmem = tmem + acc * kAccCols;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!(ok = wait_phase(full + s, ph, abort_flag, wait_limit_ns, status))) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t a = smem_u32(stage_base + s * kStageBytes);
+          const uint32_t b = a + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // advance 16 bf16 = 32 bytes along K per MMA
+            umma_bf16(d_tmem, smem_desc_sw128(a + 32 * k), smem_desc_sw128(b + 32 * k),
+                      (kb | k) != 0 ? 1u : 0u);
+          umma_commit(empty + s);  // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        umma_commit(acc_full + acc);  // the accumulator is complete once they have run
+      }
+      umma_commit(mma_done);  // arrives when every MMA issued above has completed
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // this warp may read TMEM lanes 32*quad .. 32*quad+31
+    uint32_t local = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const uint32_t acc = local & 1, use = local >> 1;
+      const bool ok = wait_phase(acc_full + acc, use & 1, abort_flag, wait_limit_ns, status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int m0 = (int)(tile / n_tiles_n) * kBM, n0 = (int)(tile % n_tiles_n) * kBN;
+      const int row = m0 + quad * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + acc * kAccCols + c * 32;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+            "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+            "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+              "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+              "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+              "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+              "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+              "=r"(v[31])
+            : "r"(taddr)
+            : "memory");
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (row < T) {
+          float4 *dst = reinterpret_cast<float4 *>(k_out + (int64_t)row * N + n0 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + acc);
+    }
   }
+
+  // ---------------------------------------------------------------- teardown
+  __syncwarp();
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
+    if (lane == 0) drain_phase(mma_done, 0, wait_limit_ns);
+    __syncwarp();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
@@ -297,18 +342,18 @@ cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out
   if (!make_map(&map_e, e, (uint64_t)T, (uint64_t)K, kBM) ||
       !make_map(&map_w, wkv, (uint64_t)N, (uint64_t)K, kBN))
     return cudaErrorInvalidValue;
-  cudaError_t err =
-      cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemBytes);
   if (err != cudaSuccess) return err;
-  const int m_tiles = (T + kBM - 1) / kBM;
-  for (int m_tile0 = 0; m_tile0 < m_tiles; m_tile0 += 65535) {  // gridDim.y limit
-    const dim3 grid(N / kBN, m_tiles - m_tile0 < 65535 ? m_tiles - m_tile0 : 65535);
-    wkv_gemm_kernel<<<grid, 128, kSmemBytes, stream>>>(map_e, map_w, k_out, T, N, K, m_tile0,
-                                                       wait_limit_ns, status);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
-  return cudaSuccess;
+  const int64_t tiles = (int64_t)((T + kBM - 1) / kBM) * (N / kBN);
+  const int grid = (int)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
+  wkv_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_e, map_w, k_out, T, N, K,
+                                                          wait_limit_ns, status);
+  return cudaGetLastError();
 }
 
 }  // namespace engram
