@@ -46,6 +46,9 @@ SMALL = {
     # a single token (the tile is almost all zero fill)
     "one_token": BASE.scaled(B=1, S=1, H=4, D=256, rows=(101, 103, 107), hash_vocab=0,
                              hidden=512),
+    # 16,684 tokens: 131 M tiles, about one tile per CTA at the end of the walk
+    "many_tiles": BASE.scaled(B=1, S=16384 + 300, H=2, D=64, rows=(1009, 1013, 1019),
+                           hash_vocab=0, dtype=W.BF16, hidden=256),
     # packed samples with image spans: dead tokens pass through
     "packed_dead": BASE.scaled(B=2, S=150, H=2, D=128, rows=(1009, 1013, 1019), hash_vocab=0,
                                hidden=256, packed=True, mean_sample_len=64, image_span=16,
