@@ -21,6 +21,7 @@ FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
 TABLE_FP8_E4M3FN, TABLE_BF16, TABLE_FP8_E8M0 = 0, 1, 2
 EID_DEAD = ROW_DEAD = -1
 LOOKUP_AUTO, LOOKUP_GATHER, LOOKUP_BULK = 0, 1, 2
+PROJECTION_AUTO, PROJECTION_SINGLE, PROJECTION_PAIR = 0, 1, 2
 MAX_HEADS, MAX_D = 32, 4096
 
 
@@ -64,6 +65,8 @@ def _load():
     L.engram_abi_version.restype = C.c_int32
     L.engram_set_lookup_kernel.argtypes = [C.c_int32]
     L.engram_set_lookup_kernel.restype = C.c_int32
+    L.engram_set_projection_kernel.argtypes = [C.c_int32]
+    L.engram_set_projection_kernel.restype = C.c_int32
     L.engram_set_wait_limit_ns.argtypes = [C.c_int64]
     L.engram_set_wait_limit_ns.restype = C.c_int64
     L.engram_debug_withhold_copies.argtypes = [C.c_int32]
@@ -371,6 +374,11 @@ def engram_status_string(code: int) -> str:
 
 def engram_abi_version() -> int:
     return int(lib.engram_abi_version())
+
+
+def engram_set_projection_kernel(which: int) -> int:
+    """PROJECTION_AUTO / PROJECTION_SINGLE / PROJECTION_PAIR; returns the previous choice."""
+    return int(lib.engram_set_projection_kernel(which))
 
 
 def engram_set_lookup_kernel(which: int) -> int:

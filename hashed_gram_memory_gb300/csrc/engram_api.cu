@@ -532,6 +532,13 @@ ENGRAM_API int32_t engram_set_lookup_kernel(int32_t which) {
   return g_lookup_kernel.exchange(which);
 }
 
+ENGRAM_API int32_t engram_set_projection_kernel(int32_t which) {
+  if (which != ENGRAM_PROJECTION_AUTO && which != ENGRAM_PROJECTION_SINGLE &&
+      which != ENGRAM_PROJECTION_PAIR)
+    return -1;
+  return engram::set_projection_kernel(which);
+}
+
 ENGRAM_API int64_t engram_set_wait_limit_ns(int64_t ns) {
   if (ns < 1000000) ns = 1000000;
   return g_wait_limit_ns.exchange(ns);

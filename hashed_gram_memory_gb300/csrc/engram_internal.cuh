@@ -70,6 +70,7 @@ cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t st
 bool bulk_supported(int D, int dtype, int H);
 
 bool wkv_gemm_supported(int N, int K);
+int set_projection_kernel(int which);  // returns the previous choice
 cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out, int T, int N, int K,
                             int64_t wait_limit_ns, int32_t *status, cudaStream_t stream);
 cudaError_t launch_concat_rows(const int32_t *row_ids, int64_t T, int H, const engram_tables &tb,

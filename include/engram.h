@@ -418,6 +418,24 @@ ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flag
 ENGRAM_API int32_t engram_set_lookup_kernel(int32_t which);
 
 /*
+ * Kernel choice of the wkv projection (engram_wkv_project, engram_connection)
+ * for this process:
+ *   ENGRAM_PROJECTION_AUTO    the library picks (default: PAIR);
+ *   ENGRAM_PROJECTION_SINGLE  one CTA per SM, 128 x 256 tiles of k, each CTA
+ *                             staging its slices of E and wkv;
+ *   ENGRAM_PROJECTION_PAIR    CTA pairs (2-CTA clusters, tcgen05 cta_group::2),
+ *                             256 x 256 tiles, each CTA staging its rows of E and
+ *                             half of the wkv slice.
+ * Both add the same products in the same order (identical results).  Returns
+ * the previous setting, or -1 for an unknown value.  Not synchronised with
+ * calls in flight on other host threads.
+ */
+#define ENGRAM_PROJECTION_AUTO 0
+#define ENGRAM_PROJECTION_SINGLE 1
+#define ENGRAM_PROJECTION_PAIR 2
+ENGRAM_API int32_t engram_set_projection_kernel(int32_t which);
+
+/*
  * Every wait inside a kernel on data another warp produces (an mbarrier phase)
  * gives up after this many nanoseconds, sets ENGRAM_FLAG_TIMEOUT and ends the
  * kernel early instead of hanging.  Default 250 ms; values below 1 ms are

@@ -264,6 +264,30 @@ def test_stages_compose_to_connection(eg):
     assert np.array_equal(E.view(torch.int16).cpu().numpy().view(np.uint16), bits)
 
 
+@pytest.mark.parametrize("name", ["bf16_h2_d64", "e8m0_h8_wide", "one_token", "many_tiles"])
+def test_projection_kernels_identical(eg, name):
+    """The CTA-pair projection (256 x 256 tiles, cta_group::2) and the one-CTA
+    projection (128 x 256 tiles) add the same products in the same order: the
+    same bits, including a lone token and a ragged last pair of tiles."""
+    import torch
+    cfg = SMALL[name]
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    rows = torch.from_numpy(oracle_rows(cfg, inp)).cuda()
+    wkv = torch.from_numpy(W.wkv_host(cfg).view(np.int16)).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    E, _ = eg.engram_concat_rows(rows, cfg.H, dev["tables"], status=st)
+    out = {}
+    try:
+        for which in (eg.PROJECTION_PAIR, eg.PROJECTION_SINGLE):
+            eg.engram_set_projection_kernel(which)
+            out[which] = eg.engram_wkv_project(E, wkv, status=st)
+    finally:
+        eg.engram_set_projection_kernel(eg.PROJECTION_AUTO)
+    assert eg.engram_read_status(st)[1] == 0
+    assert torch.equal(out[eg.PROJECTION_PAIR], out[eg.PROJECTION_SINGLE])
+
+
 def test_connection_bad_rows(eg):
     """A row id outside its table, or some (not all) ids dead, is a bad row: the
     flag is raised and that token's streams are left unwritten; the others are
