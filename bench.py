@@ -105,6 +105,16 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_burst():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"])
+    return None
+
+
 def measured_tensor_peak():
     """Dense bf16 TFLOP/s sustained under the power cap (the projection runs inside
     a seconds-long loop of steps)."""
@@ -358,6 +368,8 @@ def run_native(args):
                                "cuBLAS bf16 back to back under the power cap)",
                 "unit": "TFLOP/s",
                 "frac": t_ach / tpeak,
+                "frac_of_burst_peak": (t_ach / measured_tensor_burst()
+                                       if measured_tensor_burst() else None),
                 "traffic": recorded_traffic(cfg, "gemm"),
                 "algorithmic_flops_per_token": cfg.connection_flops_per_token(),
                 "flops_per_launch": flops,
