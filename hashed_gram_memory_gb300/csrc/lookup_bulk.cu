@@ -63,6 +63,11 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) at `src` (16-byte aligned) ahead of use.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -146,6 +151,9 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
       bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + (int64_t)ids[r] * row_bytes, row_bytes,
                bar);
     }
+    // Streams read after the rows: their HBM reads start now, under the row
+    // copies, and the loads below find them in L2.
+    if (!EARLY) prefetch_l2(p.x + t * 4 * D, (uint32_t)(8 * D));
   }
   // Meanwhile: the row scales into shared memory, the stream slices into registers.
   if (kE8) {
