@@ -1,26 +1,29 @@
 // lookup_bulk.cu -- the fused Engram lookup with the table rows staged in shared
 // memory by 1-D bulk copies (TMA), for sm_103a.
 //
-// One token per CTA of D/16 threads (16 columns each).  Thread 0 issues all 3H
-// row copies of the token at once (one contiguous D*elt-byte run per row, one
-// cp.async.bulk each) completing on a single mbarrier that expects their total
-// byte count, while the other threads fetch the row scales (or the rows'
+// One token per CTA of D/16 threads (16 columns each).  Warp 0 issues all 3H
+// row copies of the token at once, lane r the copy of row r (one contiguous
+// D*elt-byte run per row, one cp.async.bulk each, from an id the lane holds in a
+// register), completing on a single mbarrier that expects their total byte
+// count, while the other threads fetch the row scales (or the rows'
 // 32-column block exponents, 16 coalesced bytes per thread) into shared memory
 // and, for large tokens, the four 32-byte stream slices into registers with
 // evict-first loads.  After the wait every thread reads its columns of the rows
 // from shared memory, accumulates the dequantised rows in fp32, the gate sums
 // are reduced across warps, and the four streams are written back with
-// evict-first stores.  A whole token is in flight from a single issue point and
-// the rows cost no registers.  Two variants, chosen by the size of a token's
+// evict-first stores.  A whole token is in flight from one warp's issue and the
+// rows cost no registers.  Two variants, chosen by the size of a token's
 // rows: two blocks per SM with the streams loaded early (8 heads of FP8 at
 // D = 4096: 96 KB of rows), or four blocks per SM within 64 registers with the
 // streams loaded after the rows (rows within 56 KB).
 //
 // The wait is bounded by the global timer: a copy that never lands makes the
 // block set ENGRAM_FLAG_TIMEOUT, skip the token, and exit only after thread 0
-// has waited (again bounded) for the copies it issued.  An id outside its table
+// has waited (again bounded) for the copies warp 0 issued.  An id outside its table
 // makes the block set ENGRAM_FLAG_BAD_ROW and skip the token before anything
 // is copied; a dead token (all ids ENGRAM_ROW_DEAD) copies its streams through.
+#include <atomic>
+
 #include "engram_internal.cuh"
 #include "lookup_common.cuh"
 
@@ -138,22 +141,21 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
     return;  // whole block: nothing issued
   }
 
-  // Thread 0: every row copy of the token on the one barrier.
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, (uint32_t)R * row_bytes);
-    bool withhold = p.withhold != 0;
-    for (int r = 0; r < R; ++r) {
+  // Warp 0: every row copy of the token on the one barrier, lane r issuing the
+  // copies of rows r, r + 32, r + 64 from ids it loads itself (in parallel).
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)R * row_bytes);
+    __syncwarp();
+    const int withheld = p.withhold != 0 ? 0 : -1;  // test hook: row 0's copy is never issued
+    for (int r = lane; r < R; r += 32) {
       const int ni = (r >= H) + (r >= 2 * H);
-      if (withhold) {
-        withhold = false;  // test hook: this copy is never issued
-        continue;
-      }
-      bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + (int64_t)ids[r] * row_bytes, row_bytes,
-               bar);
+      const int64_t id = ids[r];
+      if (r != withheld)
+        bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
     }
     // Streams read after the rows: their HBM reads start now, under the row
     // copies, and the loads below find them in L2.
-    if (!EARLY) prefetch_l2(p.x + t * 4 * D, (uint32_t)(8 * D));
+    if (!EARLY && lane == 0) prefetch_l2(p.x + t * 4 * D, (uint32_t)(8 * D));
   }
   // Meanwhile: the row scales into shared memory, the stream slices into registers.
   if (kE8) {
@@ -264,8 +266,18 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
 template <int DT, bool AUX, bool EARLY>
 cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
   auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // The shared-memory ceiling is raised once per device to the largest any
+  // launch asks for (227 KB), not at every launch.
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
   kern<<<(unsigned)p.T, p.D / 16, smem, stream>>>(p);
   return cudaGetLastError();
 }
