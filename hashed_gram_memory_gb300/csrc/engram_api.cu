@@ -360,13 +360,17 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   p.sqrt_D = sqrtf((float)D);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   const int which = g_lookup_kernel.load(std::memory_order_relaxed);
-  const bool bulk = engram::bulk_supported(D, tb.dtype, n_heads) &&
-                    (which == ENGRAM_LOOKUP_BULK || which == ENGRAM_LOOKUP_AUTO);
-  if (bulk) {
+  const bool bulk_family = which == ENGRAM_LOOKUP_BULK || which == ENGRAM_LOOKUP_AUTO;
+  const bool bulk = bulk_family && engram::bulk_supported(D, tb.dtype, n_heads);
+  const bool small = bulk_family && !bulk && engram::bulk_small_supported(D, tb.dtype, n_heads);
+  if (bulk || small) {
     int w = g_withhold.load(std::memory_order_relaxed);
     while (w > 0 && !g_withhold.compare_exchange_weak(w, w - 1)) {
     }
     p.withhold = w > 0 ? 1 : 0;
+    if (small)
+      return launched("engram_lookup_fused launch (bulk, small rows)",
+                      engram::launch_lookup_bulk_small(p, tb.dtype, (cudaStream_t)stream));
     return launched("engram_lookup_fused launch (bulk)",
                     engram::launch_lookup_bulk(p, tb.dtype, (cudaStream_t)stream));
   }

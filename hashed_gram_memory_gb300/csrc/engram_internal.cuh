@@ -68,6 +68,8 @@ cudaError_t launch_hash(const HashParams &p, cudaStream_t stream);
 cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_supported(int D, int dtype, int H);
+cudaError_t launch_lookup_bulk_small(const LookupParams &p, int dtype, cudaStream_t stream);
+bool bulk_small_supported(int D, int dtype, int H);
 
 bool wkv_gemm_supported(int N, int K);
 int set_projection_kernel(int which);  // returns the previous choice

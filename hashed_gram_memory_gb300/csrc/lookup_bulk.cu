@@ -44,6 +44,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -263,6 +267,169 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   }
 }
 
+// Small rows (D < 512 with D/16 a power of two, e.g. the released 256-wide
+// rows): several tokens per block, each handled by its tpt = D/16 threads, which
+// issue the copies of the token's rows themselves (thread l of the token copies
+// rows l, l + tpt, ...) into the token's slot of shared memory.  Every thread
+// arrives once on the block's single mbarrier with the bytes it issued, so the
+// wait covers exactly the copies made.  The gate sums are reduced over the
+// token's threads with the same shuffles as the register-gather kernel, and
+// rows are summed in the same order: the two give identical bits.
+template <int DT, bool AUX>
+__global__ void __launch_bounds__(256, 2)
+    lookup_bulk_small_kernel(const __grid_constant__ LookupParams p) {
+  constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;
+  constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;
+  constexpr int kElt = kFp8 ? 1 : 2;
+  extern __shared__ __align__(128) uint8_t sm[];
+
+  const int H = p.H, R = 3 * H, D = p.D, tpt = p.tpt, tpb = p.tpb;
+  const uint32_t row_bytes = (uint32_t)D * kElt;
+  const uint32_t exp_bytes = kE8 ? (uint32_t)D / 32 : 0;
+  const size_t tok_bytes = (size_t)R * row_bytes;
+  uint8_t *s_rows = sm;                                            // [tpb][R][row_bytes]
+  uint8_t *s_exps = s_rows + (size_t)tpb * tok_bytes;              // [tpb][R][exp_bytes]
+  float *s_scale = reinterpret_cast<float *>(
+      s_exps + (((size_t)tpb * R * exp_bytes + 15) & ~(size_t)15));  // [tpb][R]
+  uint64_t *bar = reinterpret_cast<uint64_t *>(s_scale + (((size_t)tpb * R + 1) & ~(size_t)1));
+
+  const int tid = threadIdx.x;
+  const int tl = tid / tpt, lane_t = tid - tl * tpt;
+  const int64_t t = (int64_t)blockIdx.x * tpb + tl;
+  const bool tok_valid = t < p.T;
+  const int col0 = lane_t * 16;
+  const int32_t *ids = p.row_ids + t * R;
+
+  if (tid == 0) {
+    mbar_init(bar, blockDim.x);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();  // the barrier is set up before any thread arrives on it
+
+  // The token's state from its ids, OR-ed over its threads.
+  int bad = 0, dead = 0, live = 0;
+  if (tok_valid) {
+    for (int r = lane_t; r < R; r += tpt) {
+      const int ni = (r >= H) + (r >= 2 * H);
+      const int32_t id = ids[r];
+      if (id == ENGRAM_ROW_DEAD) {
+        dead = 1;
+      } else {
+        live = 1;
+        bad |= (id < 0) | ((int64_t)id >= p.rows[ni]);
+      }
+    }
+  }
+  for (int o = tpt >> 1; o > 0; o >>= 1) {
+    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    dead |= __shfl_xor_sync(0xffffffffu, dead, o);
+    live |= __shfl_xor_sync(0xffffffffu, live, o);
+  }
+  const bool bad_tok = tok_valid && (bad || (dead && live));
+  const bool dead_tok = tok_valid && !bad_tok && dead;
+  const bool work = tok_valid && !bad_tok && !dead_tok;
+  if (bad_tok && lane_t == 0 && p.status) atomicOr(p.status, ENGRAM_FLAG_BAD_ROW);
+
+  // This thread's rows of its token: copies, and their scales or exponents.
+  uint32_t my_bytes = 0;
+  if (work)
+    for (int r = lane_t; r < R; r += tpt) my_bytes += row_bytes;
+  if (my_bytes)
+    mbar_arrive_expect_tx(bar, my_bytes);
+  else
+    mbar_arrive(bar);
+  if (work) {
+    bool withhold = p.withhold != 0 && tid == 0;  // test hook: one copy of the block never issued
+    uint8_t *dst = s_rows + (size_t)tl * tok_bytes;
+    for (int r = lane_t; r < R; r += tpt) {
+      const int ni = (r >= H) + (r >= 2 * H);
+      const int64_t id = ids[r];
+      if (withhold)
+        withhold = false;
+      else
+        bulk_g2s(dst + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
+      if (kE8) {
+        const uint8_t *e = static_cast<const uint8_t *>(p.scale[ni]) + id * exp_bytes;
+        uint8_t *se = s_exps + ((size_t)tl * R + r) * exp_bytes;
+        for (uint32_t c = 0; c < exp_bytes; ++c) se[c] = __ldg(e + c);
+      } else if (kFp8) {
+        s_scale[(size_t)tl * R + r] = __ldg(static_cast<const float *>(p.scale[ni]) + id);
+      }
+    }
+  }
+  // The token's four stream slices, under the copies.
+  uint4 xs[4][2];
+  const uint16_t *xrow = p.x + t * 4 * D + col0;
+  if (work) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
+      xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+    }
+  }
+
+  const bool landed = wait_bounded(bar, p.wait_limit_ns);
+  // Block-uniform outcome; the barrier also publishes the scales and exponents.
+  if (__syncthreads_or(!landed)) {
+    if (tid == 0) {
+      if (p.status) atomicOr(p.status, ENGRAM_FLAG_TIMEOUT);
+      wait_bounded(bar, p.wait_limit_ns);  // let the issued copies land before exit
+    }
+    return;
+  }
+
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float saa = 0.f, smm = 0.f, sam = 0.f;
+  if (work) {
+    const uint8_t *src = s_rows + (size_t)tl * tok_bytes + (size_t)col0 * kElt;
+    for (int r = 0; r < R; ++r) {
+      const uint8_t *row = src + (size_t)r * row_bytes;
+      if (kFp8) {
+        const float scale = kE8 ? e8m0_to_float(s_exps[((size_t)tl * R + r) * exp_bytes + (col0 >> 5)])
+                                : s_scale[(size_t)tl * R + r];
+        acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), scale);
+      } else {
+        acc_bf16(acc, *reinterpret_cast<const uint4 *>(row));
+        acc_bf16(acc + 8, *reinterpret_cast<const uint4 *>(row + 16));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] *= p.inv_R;
+    gate_partials(xs[0][0], xs[0][1], acc, saa, smm, sam);
+  }
+  for (int o = tpt >> 1; o > 0; o >>= 1) {
+    saa += __shfl_xor_sync(0xffffffffu, saa, o);
+    smm += __shfl_xor_sync(0xffffffffu, smm, o);
+    sam += __shfl_xor_sync(0xffffffffu, sam, o);
+  }
+  if (!work) {
+    if (dead_tok)
+      pass_through16(p.x + t * 4 * D + col0, p.y + t * 4 * D + col0, D,
+                     AUX && p.gate_out ? p.gate_out + t : nullptr,
+                     AUX && p.mem_out ? p.mem_out + t * D + col0 : nullptr, lane_t == 0);
+    return;
+  }
+  const float g = gate_value(saa, smm, sam, (float)D, p.eps, p.sqrt_D);
+  uint16_t *yrow = p.y + t * 4 * D + col0;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const float c = g * __ldg(p.alpha + s);
+    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D), gated_add8(xs[s][0], acc, c));
+    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D + 8), gated_add8(xs[s][1], acc + 8, c));
+  }
+  if (AUX) {
+    if (p.gate_out && lane_t == 0) p.gate_out[t] = g;
+    if (p.mem_out) {
+      float4 *mo = reinterpret_cast<float4 *>(p.mem_out + t * D + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        mo[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    }
+  }
+}
+
 template <int DT, bool AUX, bool EARLY>
 cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
   auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
@@ -292,7 +459,67 @@ cudaError_t launch_bulk_dt(const LookupParams &p, size_t smem, bool aux, bool ea
              : launch_bulk_t<DT, false, false>(p, smem, stream);
 }
 
+template <int DT, bool AUX>
+cudaError_t launch_small_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
+  auto kern = lookup_bulk_small_kernel<DT, AUX>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
+  const int64_t blocks = (p.T + p.tpb - 1) / p.tpb;
+  kern<<<(unsigned)blocks, p.tpb * p.tpt, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Shared memory of the small-row kernel for tpb tokens a block.
+size_t small_smem_bytes(int D, int dtype, int H, int tpb) {
+  const size_t elt = dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
+  const size_t rows = (size_t)tpb * 3 * H;
+  const size_t exps = dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 ? rows * (D / 32) : 0;
+  return rows * D * elt + ((exps + 15) & ~(size_t)15) + ((rows + 1) & ~(size_t)1) * 4 + 8;
+}
+
+// Tokens per block: up to 256 threads, within ~113 KB of shared memory (two
+// blocks per SM), a whole number of warps.
+int small_tokens_per_block(int D, int dtype, int H) {
+  const int tpt = D / 16, warp_tokens = 32 / tpt;
+  int tpb = 256 / tpt;
+  while (tpb > warp_tokens && small_smem_bytes(D, dtype, H, tpb) > 113 * 1024) tpb -= warp_tokens;
+  return tpb;
+}
+
 }  // namespace
+
+// D below 512 with D/16 a power of two (16 .. 256) and one warp of tokens within
+// the 227 KB a block may use.
+bool bulk_small_supported(int D, int dtype, int H) {
+  if (D < 16 || D >= 512 || ((D / 16) & (D / 16 - 1)) != 0 || D % 16 != 0) return false;
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && D % 32 != 0) return false;
+  return small_smem_bytes(D, dtype, H, small_tokens_per_block(D, dtype, H)) <= 227 * 1024;
+}
+
+cudaError_t launch_lookup_bulk_small(const LookupParams &p_in, int dtype, cudaStream_t stream) {
+  if (p_in.T == 0) return cudaSuccess;
+  LookupParams p = p_in;
+  p.tpt = p.D / 16;
+  p.tpb = small_tokens_per_block(p.D, dtype, p.H);
+  const size_t smem = small_smem_bytes(p.D, dtype, p.H, p.tpb);
+  const bool aux = p.gate_out != nullptr || p.mem_out != nullptr;
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
+    return aux ? launch_small_t<ENGRAM_TABLE_FP8_E4M3FN, true>(p, smem, stream)
+               : launch_small_t<ENGRAM_TABLE_FP8_E4M3FN, false>(p, smem, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+    return aux ? launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, true>(p, smem, stream)
+               : launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, false>(p, smem, stream);
+  return aux ? launch_small_t<ENGRAM_TABLE_BF16, true>(p, smem, stream)
+             : launch_small_t<ENGRAM_TABLE_BF16, false>(p, smem, stream);
+}
 
 size_t bulk_smem_bytes(int D, int dtype, int H) {
   const size_t elt = dtype == ENGRAM_TABLE_BF16 ? 2 : 1;

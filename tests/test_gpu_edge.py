@@ -149,12 +149,16 @@ def test_zero_alpha_and_zero_rows_leave_streams_bit_identical(eg, dtype):
     assert np.all(res["mem"] == 0) and np.allclose(res["gate"], 0.5)
 
 
-def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg):
+@pytest.mark.parametrize("shape", ["one_token_a_block", "small_rows"])
+def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg, shape):
     """A withheld row copy (the mbarrier expects bytes that never come) makes the
     consumers' bounded wait run out: the launch ends by itself with
-    ENGRAM_FLAG_TIMEOUT, and the next launch on the same context is exact."""
+    ENGRAM_FLAG_TIMEOUT, and the next launch on the same context is exact.  Both
+    bulk kernels: 4096-wide rows (a token a block) and the released 256-wide rows
+    (16 tokens a block)."""
     import torch
-    cfg = W.CONFIGS[3].scaled(B=1, S=700, rows=(1009, 1013, 1019))
+    cfg = (W.CONFIGS[3].scaled(B=1, S=700, rows=(1009, 1013, 1019)) if shape == "one_token_a_block"
+           else W.CONFIGS[7].scaled(B=1, S=700, rows=(32_000,) * 3, hash_vocab=1000))
     inp = P.host_inputs(cfg)
     ref = P.oracle_path(inp)
     dev = P.to_device(inp)

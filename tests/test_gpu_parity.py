@@ -37,6 +37,10 @@ SMALL = {
                                           hash_vocab=1000, e8m0_lo=124, e8m0_hi=129),
     "release_layout_bf16_d1024": C[7].scaled(B=1, S=129, H=4, D=1024, rows=(16_000,) * 3,
                                              hash_vocab=1000, dtype=W.BF16),
+    "release_layout_d128_dead": C[7].scaled(B=2, S=211, D=128, rows=(32_000,) * 3,
+                                            hash_vocab=1000, packed=True, mean_sample_len=50,
+                                            image_span=12, image_frac=0.3),
+    "d64_bf16_h2": C[4].scaled(B=1, S=173, D=64, H=2, rows=(101, 103, 107), bf16_std=1.0),
     "packed_mm_loud_h4": C[5].scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
                                      scale_hi=1.0, mean_sample_len=40, image_span=8,
                                      image_frac=0.4),
@@ -72,7 +76,13 @@ def test_parity_vs_oracle(eg, kernel, name):
     assert np.array_equal(res2["streams"], res["streams"])
 
 
-@pytest.mark.parametrize("name", [n for n, c in SMALL.items() if c.D % 512 == 0])
+def _bulk_shape(c):
+    """Shapes the bulk kernels take: D a multiple of 512 (one token a block), or
+    D/16 a power of two below 512 (several tokens a block)."""
+    return c.D % 512 == 0 or (c.D < 512 and (c.D // 16) & (c.D // 16 - 1) == 0)
+
+
+@pytest.mark.parametrize("name", [n for n, c in SMALL.items() if _bulk_shape(c)])
 def test_bulk_and_gather_kernels_agree_bit_for_bit(eg, name):
     cfg = SMALL[name]
     dev = P.to_device(P.host_inputs(cfg))
