@@ -485,12 +485,13 @@ size_t small_smem_bytes(int D, int dtype, int H, int tpb) {
   return rows * D * elt + ((exps + 15) & ~(size_t)15) + ((rows + 1) & ~(size_t)1) * 4 + 8;
 }
 
-// Tokens per block: up to 256 threads, within ~113 KB of shared memory (two
-// blocks per SM), a whole number of warps.
+// Tokens per block: up to 256 threads, within 56 KB of shared memory (four
+// blocks per SM: their copy, compute and store phases overlap better than two
+// larger blocks'), a whole number of warps.
 int small_tokens_per_block(int D, int dtype, int H) {
   const int tpt = D / 16, warp_tokens = 32 / tpt;
   int tpb = 256 / tpt;
-  while (tpb > warp_tokens && small_smem_bytes(D, dtype, H, tpb) > 113 * 1024) tpb -= warp_tokens;
+  while (tpb > warp_tokens && small_smem_bytes(D, dtype, H, tpb) > 56 * 1024) tpb -= warp_tokens;
   return tpb;
 }
 
