@@ -20,7 +20,7 @@ import workloads as W  # noqa: E402
 
 
 def tiny_results():
-    cfg = W.CONFIGS[0]
+    cfg = W.by_name("tiny_fp8_d256")
     ids = W.token_ids(cfg)
     eids, f1 = oracle.compress(ids, W.tid2eid(cfg), cfg.n_eids)
     rows, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows)
@@ -40,7 +40,7 @@ def digest(a) -> str:
 def summary():
     r = tiny_results()
     return {
-        "workload": W.CONFIGS[0].name,
+        "workload": W.by_name("tiny_fp8_d256").name,
         "flags": r["flags"],
         "sha256": {k: digest(r[k]) for k in ("eids", "rows", "streams_out")},
         "inputs_sha256": {k: digest(v) for k, v in r["inputs"].items()},

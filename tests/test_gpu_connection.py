@@ -29,7 +29,7 @@ pytestmark = pytest.mark.gpu
 
 FILL = 0x1234   # pre-filled output: bad tokens must leave it unwritten
 
-BASE = W.CONFIGS[8]
+BASE = W.by_name("release_connection_e8m0")
 SMALL = {
     # BF16 tables, K = 3*2*64 = 384, hidden 256 (one N tile), 300 tokens (3 M tiles, ragged)
     "bf16_h2_d64": BASE.scaled(B=1, S=300, H=2, D=64, rows=(1009, 1013, 1019), hash_vocab=0,

@@ -28,8 +28,8 @@ def _t(a):
 
 def test_empty_inputs(eg):
     import torch
-    cfg = W.CONFIGS[0].scaled(S=0)
-    inp = P.host_inputs(W.CONFIGS[0])
+    cfg = W.by_name("tiny_fp8_d256").scaled(S=0)
+    inp = P.host_inputs(W.by_name("tiny_fp8_d256"))
     dev = P.to_device(inp)
     e = eg.engram_compress(torch.zeros((1, 0), dtype=torch.int32, device="cuda"), dev["tid2eid"], 800)
     assert e.numel() == 0
@@ -76,7 +76,7 @@ def test_hash_flags_negative_ids_and_unwritten(eg):
 
 def test_lookup_flags_bad_rows_and_leaves_token_unwritten(eg):
     import torch
-    cfg = W.CONFIGS[0].scaled(S=37)
+    cfg = W.by_name("tiny_fp8_d256").scaled(S=37)
     inp = P.host_inputs(cfg)
     eids, _ = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
     rows, _ = oracle.hash_ids(eids, cfg.H, cfg.rows)
@@ -102,7 +102,7 @@ def test_lookup_flags_bad_rows_and_leaves_token_unwritten(eg):
 @pytest.mark.parametrize("split", [0, 1, 2, 3, 9])
 def test_decode_steps_in_place_history_equal_prefill(eg, split):
     import torch
-    cfg = W.CONFIGS[2].scaled(B=5, S=1, rows=(5_040_000,) * 3)
+    cfg = W.by_name("decode_fp8").scaled(B=5, S=1, rows=(5_040_000,) * 3)
     g = np.random.default_rng(17 + split)
     S = 14
     eids = g.integers(1, 100_000, size=(cfg.B, S)).astype(np.int32)
@@ -134,7 +134,7 @@ def test_two_token_step_in_place_history(eg):
 @pytest.mark.parametrize("dtype", [W.FP8, W.BF16])
 def test_zero_alpha_and_zero_rows_leave_streams_bit_identical(eg, dtype):
     import torch
-    base = W.CONFIGS[0] if dtype == W.FP8 else W.CONFIGS[4].scaled(B=1, S=64, rows=(97, 89, 83))
+    base = W.by_name("tiny_fp8_d256") if dtype == W.FP8 else W.by_name("bf16_tables").scaled(B=1, S=64, rows=(97, 89, 83))
     inp = P.host_inputs(base)
     assert not (inp.streams == 0x8000).any()
     dev = P.to_device(inp)
@@ -157,8 +157,8 @@ def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg, shape):
     bulk kernels: 4096-wide rows (a token a block) and the released 256-wide rows
     (16 tokens a block)."""
     import torch
-    cfg = (W.CONFIGS[3].scaled(B=1, S=700, rows=(1009, 1013, 1019)) if shape == "one_token_a_block"
-           else W.CONFIGS[7].scaled(B=1, S=700, rows=(32_000,) * 3, hash_vocab=1000))
+    cfg = (W.by_name("full_prefill_fp8").scaled(B=1, S=700, rows=(1009, 1013, 1019)) if shape == "one_token_a_block"
+           else W.by_name("release_layout_fp8").scaled(B=1, S=700, rows=(32_000,) * 3, hash_vocab=1000))
     inp = P.host_inputs(cfg)
     ref = P.oracle_path(inp)
     dev = P.to_device(inp)

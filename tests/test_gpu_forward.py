@@ -22,10 +22,10 @@ def eg():
 
 
 CASES = {
-    "prefill_h8": W.CONFIGS[3].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
-    "decode_history": W.CONFIGS[2].scaled(B=300, rows=(7001, 7013, 7019)),
-    "bf16": W.CONFIGS[4].scaled(B=3, S=133, rows=(3001, 3011, 3019)),
-    "tiny_d256": W.CONFIGS[0],
+    "prefill_h8": W.by_name("full_prefill_fp8").scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "decode_history": W.by_name("decode_fp8").scaled(B=300, rows=(7001, 7013, 7019)),
+    "bf16": W.by_name("bf16_tables").scaled(B=3, S=133, rows=(3001, 3011, 3019)),
+    "tiny_d256": W.by_name("tiny_fp8_d256"),
 }
 
 

@@ -11,37 +11,37 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-C = W.CONFIGS
+C = W.by_name
 SMALL = {
-    "tiny_fp8_d256": C[0],
-    "mid_prefill_fp8": C[1].scaled(B=2, S=301, rows=(4099, 5003, 6007)),
-    "decode_fp8": C[2].scaled(B=300, rows=(7001, 7013, 7019)),
-    "full_prefill_fp8": C[3].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
-    "bf16_tables": C[4].scaled(B=3, S=133, rows=(3001, 3011, 3019)),
-    "loud_fp8": C[3].scaled(B=1, S=211, rows=(1009, 1013, 1019), scale_lo=0.5, scale_hi=1.0),
-    "loud_bf16": C[4].scaled(B=1, S=199, rows=(1009, 1013, 1019), bf16_std=1.0),
-    "d48_h1": C[0].scaled(S=97, D=48, H=1, rows=(11, 13, 17)),
-    "d1040_h5": C[1].scaled(B=1, S=77, D=1040, H=5, rows=(101, 103, 107), scale_lo=0.5,
+    "tiny_fp8_d256": C("tiny_fp8_d256"),
+    "mid_prefill_fp8": C("mid_prefill_fp8").scaled(B=2, S=301, rows=(4099, 5003, 6007)),
+    "decode_fp8": C("decode_fp8").scaled(B=300, rows=(7001, 7013, 7019)),
+    "full_prefill_fp8": C("full_prefill_fp8").scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "bf16_tables": C("bf16_tables").scaled(B=3, S=133, rows=(3001, 3011, 3019)),
+    "loud_fp8": C("full_prefill_fp8").scaled(B=1, S=211, rows=(1009, 1013, 1019), scale_lo=0.5, scale_hi=1.0),
+    "loud_bf16": C("bf16_tables").scaled(B=1, S=199, rows=(1009, 1013, 1019), bf16_std=1.0),
+    "d48_h1": C("tiny_fp8_d256").scaled(S=97, D=48, H=1, rows=(11, 13, 17)),
+    "d1040_h5": C("mid_prefill_fp8").scaled(B=1, S=77, D=1040, H=5, rows=(101, 103, 107), scale_lo=0.5,
                             scale_hi=1.0),
-    "d16_h32_bf16": C[4].scaled(B=2, S=41, D=16, H=32, rows=(1, 2, 3), bf16_std=1.0),
-    "d4096_h32": C[3].scaled(B=1, S=19, H=32, rows=(50, 60, 70)),
-    "d2560_decode": C[2].scaled(B=37, D=2560, rows=(97, 89, 83)),
-    "packed_mm_fp8": C[5].scaled(B=2, S=611, rows=(4099, 5003, 6007), mean_sample_len=90,
+    "d16_h32_bf16": C("bf16_tables").scaled(B=2, S=41, D=16, H=32, rows=(1, 2, 3), bf16_std=1.0),
+    "d4096_h32": C("full_prefill_fp8").scaled(B=1, S=19, H=32, rows=(50, 60, 70)),
+    "d2560_decode": C("decode_fp8").scaled(B=37, D=2560, rows=(97, 89, 83)),
+    "packed_mm_fp8": C("packed_mm_fp8").scaled(B=2, S=611, rows=(4099, 5003, 6007), mean_sample_len=90,
                                  image_span=24),
-    "e8m0_prefill_h8": C[6].scaled(B=2, S=517, rows=(6007, 6011, 6029)),
-    "e8m0_loud_h4_d1024": C[6].scaled(B=1, S=233, H=4, D=1024, rows=(1009, 1013, 1019),
+    "e8m0_prefill_h8": C("full_prefill_fp8_e8m0").scaled(B=2, S=517, rows=(6007, 6011, 6029)),
+    "e8m0_loud_h4_d1024": C("full_prefill_fp8_e8m0").scaled(B=1, S=233, H=4, D=1024, rows=(1009, 1013, 1019),
                                       e8m0_lo=124, e8m0_hi=129),
-    "e8m0_d96": C[6].scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41)),
-    "release_layout_d256": C[7].scaled(B=2, S=333, rows=(32_000,) * 3, hash_vocab=1000),
-    "release_layout_d512_h4": C[7].scaled(B=1, S=301, H=4, D=512, rows=(16_000,) * 3,
+    "e8m0_d96": C("full_prefill_fp8_e8m0").scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41)),
+    "release_layout_d256": C("release_layout_fp8").scaled(B=2, S=333, rows=(32_000,) * 3, hash_vocab=1000),
+    "release_layout_d512_h4": C("release_layout_fp8").scaled(B=1, S=301, H=4, D=512, rows=(16_000,) * 3,
                                           hash_vocab=1000, e8m0_lo=124, e8m0_hi=129),
-    "release_layout_bf16_d1024": C[7].scaled(B=1, S=129, H=4, D=1024, rows=(16_000,) * 3,
+    "release_layout_bf16_d1024": C("release_layout_fp8").scaled(B=1, S=129, H=4, D=1024, rows=(16_000,) * 3,
                                              hash_vocab=1000, dtype=W.BF16),
-    "release_layout_d128_dead": C[7].scaled(B=2, S=211, D=128, rows=(32_000,) * 3,
+    "release_layout_d128_dead": C("release_layout_fp8").scaled(B=2, S=211, D=128, rows=(32_000,) * 3,
                                             hash_vocab=1000, packed=True, mean_sample_len=50,
                                             image_span=12, image_frac=0.3),
-    "d64_bf16_h2": C[4].scaled(B=1, S=173, D=64, H=2, rows=(101, 103, 107), bf16_std=1.0),
-    "packed_mm_loud_h4": C[5].scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
+    "d64_bf16_h2": C("bf16_tables").scaled(B=1, S=173, D=64, H=2, rows=(101, 103, 107), bf16_std=1.0),
+    "packed_mm_loud_h4": C("packed_mm_fp8").scaled(B=3, S=257, H=4, rows=(1009, 1013, 1019), scale_lo=0.5,
                                      scale_hi=1.0, mean_sample_len=40, image_span=8,
                                      image_frac=0.4),
 }

@@ -204,7 +204,7 @@ def test_history_out_short_sequences_and_aliasing_safe():
 
 
 def test_identical_windows_identical_rows_on_planted_repeats():
-    cfg = W.CONFIGS[3].scaled(B=2, S=512)
+    cfg = W.by_name("full_prefill_fp8").scaled(B=2, S=512)
     ids = W.token_ids(cfg)
     planted = W.plant_repeats(ids.copy(), cfg.repeat_frac, W.rng(cfg, 7, 0))
     assert len(planted) == 2 * round(0.05 * 512 / 4)

@@ -43,7 +43,7 @@ def _worker(rank, world, port, out):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    cfg = W.CONFIGS[0].scaled(B=5, S=24)
+    cfg = W.by_name("tiny_fp8_d256").scaled(B=5, S=24)
     ids = W.token_ids(cfg)
     b0, b1 = shard_range(cfg.B, rank, world)
     e, _ = oracle.compress(ids[b0:b1], W.tid2eid(cfg), cfg.n_eids)
@@ -64,7 +64,7 @@ def test_two_gloo_ranks_reassemble_the_batch():
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, join=True,
                        start_method="spawn")
-    cfg = W.CONFIGS[0].scaled(B=5, S=24)
+    cfg = W.by_name("tiny_fp8_d256").scaled(B=5, S=24)
     e, _ = oracle.compress(W.token_ids(cfg), W.tid2eid(cfg), cfg.n_eids)
     full, _ = oracle.hash_ids(e, cfg.H, cfg.rows)
     parts = []

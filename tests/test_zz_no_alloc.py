@@ -38,8 +38,8 @@ def _static_call(eg, cfg, dev, out, status, stream):
 
 def test_static_entry_point_matches_forward_on_two_calls(eg):
     import torch
-    cases = [W.CONFIGS[3].scaled(B=2, S=517, rows=(6007, 6011, 6029)),       # prefill, 8 heads
-             W.CONFIGS[2].scaled(B=300, rows=(7001, 7013, 7019))]           # decode with history
+    cases = [W.by_name("full_prefill_fp8").scaled(B=2, S=517, rows=(6007, 6011, 6029)),       # prefill, 8 heads
+             W.by_name("decode_fp8").scaled(B=300, rows=(7001, 7013, 7019))]           # decode with history
     stream = torch.cuda.Stream()
     for i, cfg in enumerate(cases):
         inp = P.host_inputs(cfg, rank=i)
@@ -61,7 +61,7 @@ def test_static_entry_point_matches_forward_on_two_calls(eg):
 
 def test_static_entry_point_rejects_oversized_requests(eg):
     import torch
-    cfg = W.CONFIGS[3].scaled(B=64, S=8192, rows=(11, 13, 17))   # 524,288 tokens at 8 heads
+    cfg = W.by_name("full_prefill_fp8").scaled(B=64, S=8192, rows=(11, 13, 17))   # 524,288 tokens at 8 heads
     need = eg.engram_forward_workspace_bytes(cfg.B, cfg.S, cfg.H)
     assert need > eg.STATIC_WORKSPACE_BYTES
     dev = dict(ids=torch.zeros((cfg.B, cfg.S), dtype=torch.int32, device="cuda"),

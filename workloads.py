@@ -163,6 +163,14 @@ CONFIGS = [
 ]
 
 
+def by_name(name: str) -> EngramConfig:
+    """The workload of that name."""
+    for c in CONFIGS:
+        if c.name == name:
+            return c
+    raise KeyError(name)
+
+
 def rng(cfg: EngramConfig, kind: int, sub: int = 0) -> np.random.Generator:
     return np.random.default_rng([cfg.seed, kind, sub])
 
