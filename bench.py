@@ -80,6 +80,32 @@ def config_of(name: str, args=None) -> W.EngramConfig:
     return cfg
 
 
+L2_BYTES = 126 * 2**20   # GB300 L2
+
+
+def stream_rotation(cfg: W.EngramConfig, l2_bytes: int = L2_BYTES) -> int:
+    """How many separate stream buffers the timed steps cycle through, so that a
+    step never finds its input streams in L2: one when a step's streams (in +
+    out) already exceed twice the L2, else enough copies to exceed it."""
+    per_step = cfg.T * 4 * cfg.width * 2 * 2
+    if per_step >= 2 * l2_bytes:
+        return 1
+    return min(256, -(-2 * l2_bytes // per_step))
+
+
+def l2_note(cfg: W.EngramConfig, l2_bytes: int = L2_BYTES) -> str:
+    per_step = cfg.T * 4 * cfg.width * 2
+    n = stream_rotation(cfg, l2_bytes)
+    if n == 1:
+        return (f"no flush: every input is larger than the {l2_bytes / 2**20:.0f} MiB L2 (tables "
+                f"{cfg.table_bytes() / 2**30:.1f} GiB; streams {per_step / 1e9:.3f} GB read and "
+                f"{per_step / 1e9:.3f} GB written per step)")
+    return (f"inputs larger than L2 by rotation: the streams of a step ({per_step / 1e6:.1f} MB "
+            f"read, as many written) fit in the {l2_bytes / 2**20:.0f} MiB L2, so the timed steps cycle "
+            f"through {n} separate input and output buffers ({2 * n * per_step / 1e6:.0f} MB); "
+            f"tables {cfg.table_bytes() / 2**30:.1f} GiB")
+
+
 def workload_desc(cfg: W.EngramConfig) -> dict:
     d = {
         "workload": cfg.name,
@@ -87,9 +113,7 @@ def workload_desc(cfg: W.EngramConfig) -> dict:
         "table_rows": list(cfg.rows), "table_dtype": cfg.dtype,
         "table_bytes": cfg.table_bytes(), "token_ids": cfg.ids,
         "repeated_4gram_frac": cfg.repeat_frac, "decode_history": cfg.decode,
-        "l2": "no flush: every input is larger than the 129 MB L2 "
-              f"(tables {cfg.table_bytes() / 2**30:.1f} GiB, streams "
-              f"{cfg.T * 4 * cfg.width * 2 / 1e9:.2f} GB in + out per step)",
+        "l2": l2_note(cfg),
         "parallelism": "replicas (weak scaling, no data-path collective)",
     }
     if cfg.hidden:
@@ -327,6 +351,10 @@ def run_native(args):
         raise SystemExit(f"device status flags 0x{flags:x} during warm-up")
 
     K = args.steps
+    # Streams that fit in L2 rotate among separate buffers (see stream_rotation).
+    n_rot = stream_rotation(cfg)
+    xs_rot = [d["streams"]] + [d["streams"].clone() for _ in range(n_rot - 1)]
+    ys_rot = [step.out] + [torch.empty_like(step.out) for _ in range(n_rot - 1)]
     # The K timed steps are captured once into a CUDA graph and replayed, so the
     # GPU runs them back to back without waiting on Python between launches;
     # the events around each dominant-kernel launch are graph nodes that record
@@ -340,7 +368,7 @@ def run_native(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(K):
-                step(ev[i][0], ev[i][1])
+                step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
         with torch.cuda.stream(stream):
             graph.replay()   # untimed: the graph's first launch uploads it
         torch.cuda.synchronize()
@@ -356,7 +384,7 @@ def run_native(args):
             graph.replay()
     else:
         for i in range(K):
-            step(ev[i][0], ev[i][1])
+            step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
     t_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
