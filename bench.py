@@ -272,6 +272,14 @@ class Step:
         self.primes = (eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0]
                        if cfg.hash_vocab else None)
         self.launches = 3
+        # One new token a slot: the one-call engram_forward, which runs the decode
+        # step as one fused launch (compress, window, hash and lookup).
+        self.fused_decode = (cfg.S == 1 and not cfg.packed and not cfg.hidden and
+                             cfg.D % 512 == 0 and args_lookup_kernel() != "gather")
+        if self.fused_decode:
+            self.ws = torch.empty(max(16, eg.engram_forward_workspace_bytes(cfg.B, cfg.S, cfg.H)),
+                                  dtype=torch.uint8, device=dev)
+            self.launches = 1
         if cfg.hidden:   # the connection: concat rows, project, gate + add
             self.e = torch.empty((cfg.T, cfg.K), dtype=torch.bfloat16, device=dev)
             self.state = torch.empty((cfg.T,), dtype=torch.uint8, device=dev)
@@ -283,6 +291,16 @@ class Step:
         ids = d["ids"] if ids is None else ids
         x = d["streams"] if x is None else x
         out = self.out if out is None else out
+        if self.fused_decode:
+            if ev_start is not None:
+                ev_start.record(self.stream)
+            eg.engram_forward(ids, d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], x, d["alpha"],
+                              cfg.eps, history=d["history"], history_out=self.hist_out,
+                              streams_out=out, workspace=self.ws, status=self.status,
+                              stream=self.stream)
+            if ev_end is not None:
+                ev_end.record(self.stream)
+            return
         eg.engram_compress(ids, d["tid2eid"], cfg.n_eids, eids_out=self.eids, status=self.status,
                            stream=self.stream, dead=d["dead"])
         eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
@@ -318,6 +336,13 @@ def graph_timing_supported() -> bool:
         return False
 
 
+_LOOKUP_KERNEL = ["auto"]
+
+
+def args_lookup_kernel() -> str:
+    return _LOOKUP_KERNEL[0]
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -335,6 +360,7 @@ def run_native(args):
         dist.init_process_group("nccl", device_id=device)
 
     cfg = config_of(args.workload, args)
+    _LOOKUP_KERNEL[0] = args.lookup_kernel
     eg.engram_set_lookup_kernel({"auto": eg.LOOKUP_AUTO, "gather": eg.LOOKUP_GATHER,
                                  "bulk": eg.LOOKUP_BULK}[args.lookup_kernel])
     d = device_inputs(eg, cfg, rank, device)
@@ -413,6 +439,10 @@ def run_native(args):
         # a dead token moves its row ids and a copy of its streams, no table rows
         bytes_dead = cfg.R * 4 + 2 * 4 * cfg.width * 2
         bytes_tok = (cfg.algorithmic_bytes_per_token() * (cfg.T - n_dead) + bytes_dead * n_dead) / cfg.T
+        if step.fused_decode:
+            # the fused step keeps the row ids on chip and moves a token id, its map
+            # entry and the slot's history in and out instead
+            bytes_tok += 4 + 4 + 12 + 12 - cfg.R * 4
         lk = statistics.mean(lookup_ms)
         achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
         traffic = recorded_traffic(cfg, args.lookup_kernel)
@@ -455,7 +485,8 @@ def run_native(args):
             "config": workload_desc(cfg),
             "hbm_gbs_effective_step": bytes_tok * cfg.T * K / (ms_total * 1e-3) / 1e9,
             "roofline": roof if cfg.hidden else {
-                "kernel": "engram_lookup_fused",
+                "kernel": ("engram_forward (decode_step_kernel: compress, hash and lookup fused)"
+                           if step.fused_decode else "engram_lookup_fused"),
                 "lookup_kernel": args.lookup_kernel,
                 "bound": "hbm",
                 "achieved": achieved,

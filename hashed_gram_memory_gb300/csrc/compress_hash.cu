@@ -7,20 +7,10 @@
 // row id (hash), with the 3H threads of a token in one block so that the ids of
 // its window are read once from L1.
 #include "engram_internal.cuh"
+#include "hash_device.cuh"
 
 namespace engram {
 namespace {
-
-constexpr uint64_t kFold = 0x9E3779B97F4A7C15ull;
-
-// x mod d for d >= 1, with m = floor((2^64 - 1) / d).  q = umulhi(x, m) is
-// floor(x/d) or one less (d*m lies within d of 2^64, so x*m/2^64 > x/d - 1), so
-// x - q*d is in [0, 2d) and one conditional subtraction finishes it.
-__device__ __forceinline__ uint64_t mod_by_reciprocal(uint64_t x, uint64_t d, uint64_t m) {
-  const uint64_t q = __umul64hi(x, m);
-  const uint64_t r = x - q * d;
-  return r >= d ? r - d : r;
-}
 
 __device__ __forceinline__ void flag_warp(int32_t *status, uint32_t flags) {
   // One atomic per warp instead of one per thread.
@@ -82,41 +72,17 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
     const int32_t self = raw[3];
     bool dead = self == ENGRAM_EID_DEAD, bad = self < ENGRAM_EID_DEAD;
     if (!dead && !bad) {
-      w[3] = self;
+      // positions before 0 hold the history or 0 (raw), so the limit alone decides
       const int64_t limit = p.positions ? (int64_t)p.positions[base + s] : (p.history ? 3 : s);
-      bool blocked = false;
-#pragma unroll
-      for (int k = 1; k <= 3; ++k) {
-        int32_t e = 0;
-        if (!blocked && k <= limit && (s - k >= 0 || p.history)) {
-          e = raw[3 - k];
-          if (e == ENGRAM_EID_DEAD) {
-            blocked = true;
-            e = 0;
-          } else if (e < 0) {
-            bad = true;
-          }
-        }
-        w[3 - k] = e;
-      }
+      const int32_t before[3] = {raw[0], raw[1], raw[2]};
+      bad = !make_window(before, self, limit, w);
     }
     if (bad) {
       flags = ENGRAM_FLAG_BAD_EID;
     } else if (dead) {
       p.row_ids[t * R + r] = ENGRAM_ROW_DEAD;
     } else {
-      const int ni = (r >= p.H) + (r >= 2 * p.H);  // n - 2
-      const int j = r - ni * p.H;
-      uint64_t h = p.seed[ni][j];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {  // the last n = ni + 2 ids, oldest first
-        if (k >= 2 - ni) {
-          h = (h ^ (uint64_t)(uint32_t)w[k]) * kFold;
-          h ^= h >> 29;
-        }
-      }
-      p.row_ids[t * R + r] =
-          (int32_t)(p.off[ni][j] + mod_by_reciprocal(h, p.mod[ni][j], p.rmul[ni][j]));
+      p.row_ids[t * R + r] = window_row(w, r, p.H, p.seed, p.mod, p.rmul, p.off);
     }
   }
   flag_warp(p.status, flags);

@@ -278,12 +278,19 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
                             row_ids_out, status, stream);
 }
 
-ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
-                                             int32_t n_heads, const engram_tables *tables_host,
-                                             const uint16_t *streams_in, uint16_t *streams_out,
-                                             const float *alpha, float eps, float *gate_out,
-                                             float *mem_out, int32_t *status, void *stream) {
-  const char *fn = "engram_lookup_fused";
+}  // extern "C"
+
+// The argument checks of engram_lookup_fused and the fill of its launch
+// parameters; row_ids may be NULL when `need_row_ids` is false (the fused
+// decode step makes them itself).  With n_tokens == 0 it returns OK without a
+// device query and leaves p.T == 0.
+engram_status engram::prepare_lookup(const char *fn, const int32_t *row_ids, bool need_row_ids,
+                                     int64_t n_tokens, int32_t n_heads,
+                                     const engram_tables *tables_host, const uint16_t *streams_in,
+                                     uint16_t *streams_out, const float *alpha, float eps,
+                                     float *gate_out, float *mem_out, int32_t *status,
+                                     LookupParams &p) {
+  memset(&p, 0, sizeof p);
   if (n_tokens < 0) return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens < 0", fn);
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
@@ -317,7 +324,7 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   const size_t R = 3 * (size_t)n_heads;
   const size_t sbytes = (size_t)n_tokens * 4 * D * 2;
   if (n_tokens > 0) {
-    if (!row_ids || !streams_in || !streams_out)
+    if ((need_row_ids && !row_ids) || !streams_in || !streams_out)
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids or streams is NULL", fn);
     if (!aligned(row_ids, 4) || !aligned(status, 4) || !aligned(gate_out, 4))
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: row_ids/status/gate_out not 4-byte aligned", fn);
@@ -337,8 +344,6 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   if (n_tokens == 0) return ok();
   engram_status st = check_device();
   if (st != ENGRAM_OK) return st;
-  engram::LookupParams p;
-  memset(&p, 0, sizeof p);
   p.row_ids = row_ids;
   for (int n = 0; n < 3; ++n) {
     p.table[n] = static_cast<const uint8_t *>(tb.table[n]);
@@ -359,6 +364,25 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   p.inv_D = 1.f / (float)D;
   p.sqrt_D = sqrtf((float)D);
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return ENGRAM_OK;
+}
+
+int engram::lookup_kernel_choice() { return g_lookup_kernel.load(std::memory_order_relaxed); }
+
+extern "C" {
+
+ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
+                                             int32_t n_heads, const engram_tables *tables_host,
+                                             const uint16_t *streams_in, uint16_t *streams_out,
+                                             const float *alpha, float eps, float *gate_out,
+                                             float *mem_out, int32_t *status, void *stream) {
+  engram::LookupParams p;
+  engram_status st =
+      engram::prepare_lookup("engram_lookup_fused", row_ids, true, n_tokens, n_heads, tables_host,
+                             streams_in, streams_out, alpha, eps, gate_out, mem_out, status, p);
+  if (st != ENGRAM_OK || n_tokens == 0) return st;
+  const engram_tables &tb = *tables_host;
+  const int D = tb.D;
   const int which = g_lookup_kernel.load(std::memory_order_relaxed);
   const bool bulk_family = which == ENGRAM_LOOKUP_BULK || which == ENGRAM_LOOKUP_AUTO;
   const bool bulk = bulk_family && engram::bulk_supported(D, tb.dtype, n_heads);

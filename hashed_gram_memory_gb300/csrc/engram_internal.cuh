@@ -63,11 +63,27 @@ struct LookupParams {
   float eps, inv_R, inv_D, sqrt_D;
 };
 
+// The fused decode step: compress + window + hash + bulk lookup, one slot a block.
+struct DecodeParams {
+  LookupParams lk;           // row_ids unused
+  const int32_t *token_ids;  // [batch] (one new token a slot)
+  const int32_t *tid2eid;
+  const int32_t *history;    // [batch, 3] oldest first, or NULL (pad)
+  int32_t *history_out;      // [batch, 3] or NULL; may be history
+  int32_t *row_ids_out;      // [batch, 3H] or NULL
+  int32_t vocab, n_eids;
+  uint64_t mod[3][kMaxHeads];
+  uint64_t off[3][kMaxHeads];
+  uint64_t rmul[3][kMaxHeads];
+  uint64_t seed[3][kMaxHeads];
+};
+
 cudaError_t launch_compress(const CompressParams &p, cudaStream_t stream);
 cudaError_t launch_hash(const HashParams &p, cudaStream_t stream);
 cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_supported(int D, int dtype, int H);
+cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk_small(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_small_supported(int D, int dtype, int H);
 
@@ -85,6 +101,13 @@ cudaError_t launch_connection(const int32_t *row_ids, int64_t T, int H, const en
                               const float *alpha, float eps, uint16_t *e, float *k,
                               uint8_t *state, float *gate_out, int64_t wait_limit_ns,
                               int32_t *status, cudaStream_t stream);
+
+engram_status prepare_lookup(const char *fn, const int32_t *row_ids, bool need_row_ids,
+                             int64_t n_tokens, int32_t n_heads, const engram_tables *tables_host,
+                             const uint16_t *streams_in, uint16_t *streams_out, const float *alpha,
+                             float eps, float *gate_out, float *mem_out, int32_t *status,
+                             LookupParams &p);
+int lookup_kernel_choice();
 
 // Records the message engram_last_error() returns on this thread; returns code.
 engram_status set_error(engram_status code, const char *fmt, ...);

@@ -45,6 +45,65 @@ engram_status fwd_fail(engram_status code, const char *msg) {
   return engram::set_error(code, "%s", msg);
 }
 
+bool misaligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) != 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// One decode step (one new token a slot) in one launch: compression, window,
+// hash and bulk lookup fused, with the same argument checks as the three
+// calls it replaces.  The row ids are not written out.
+engram_status decode_step(const int32_t *token_ids, int32_t batch, const int32_t *tid2eid,
+                          int32_t vocab, int32_t n_eids, const int32_t *history,
+                          int32_t *history_out, int32_t n_heads, const engram_tables *tables_host,
+                          const uint16_t *streams_in, uint16_t *streams_out, const float *alpha,
+                          float eps, int32_t *status, void *stream) {
+  const char *fn = "engram_forward";
+  if (!token_ids || !tid2eid || misaligned4(token_ids) || misaligned4(tid2eid))
+    return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: token_ids or tid2eid NULL or misaligned");
+  if (vocab < 1 || n_eids < 0)
+    return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: vocab must be >= 1 and n_eids >= 0");
+  if (misaligned4(history) || misaligned4(history_out))
+    return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: history pointers not 4-byte aligned");
+  const size_t hb = (size_t)batch * 12;
+  const size_t sb = (size_t)batch * 4 * tables_host->D * 2;
+  if (history && history_out && history != history_out && overlaps(history, hb, history_out, hb))
+    return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: history and history_out overlap partially");
+  if (history_out && (overlaps(history_out, hb, streams_out, sb) ||
+                      overlaps(history_out, hb, token_ids, (size_t)batch * 4)))
+    return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: history_out overlaps another buffer");
+  for (int n = 0; n < 3; ++n)
+    if (tables_host->rows[n] < 1 || tables_host->rows[n] > INT32_MAX)
+      return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: rows must be in [1, 2^31-1]");
+  engram::DecodeParams p;
+  memset(&p, 0, sizeof p);
+  engram_status st =
+      engram::prepare_lookup(fn, nullptr, false, batch, n_heads, tables_host, streams_in,
+                             streams_out, alpha, eps, nullptr, nullptr, status, p.lk);
+  if (st != ENGRAM_OK) return st;
+  p.token_ids = token_ids;
+  p.tid2eid = tid2eid;
+  p.history = history;
+  p.history_out = history_out;
+  p.vocab = vocab;
+  p.n_eids = n_eids;
+  for (int n = 0; n < 3; ++n)
+    for (int j = 0; j < n_heads; ++j) {
+      p.mod[n][j] = (uint64_t)tables_host->rows[n];
+      p.off[n][j] = 0;
+      p.rmul[n][j] = UINT64_MAX / p.mod[n][j];
+      p.seed[n][j] = engram::splitmix64((uint64_t)((n + 2) * 16 + j));
+    }
+  const cudaError_t e = engram::launch_decode_step(p, tables_host->dtype, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return engram::set_error(ENGRAM_ERR_CUDA, "engram_forward decode launch: %s",
+                             cudaGetErrorString(e));
+  return ENGRAM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -70,6 +129,13 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
     return fwd_fail(ENGRAM_ERR_INVALID_ARG,
                     "engram_forward: workspace NULL, misaligned or smaller than "
                     "engram_forward_workspace_bytes()");
+  if (seq == 1 && T > 0) {
+    const int which = engram::lookup_kernel_choice();
+    if ((which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
+        engram::bulk_supported(tables_host->D, tables_host->dtype, n_heads))
+      return decode_step(token_ids, batch, tid2eid, vocab, n_eids, history, history_out, n_heads,
+                         tables_host, streams_in, streams_out, alpha, eps, status, stream);
+  }
   int32_t *eids = static_cast<int32_t *>(workspace);
   int32_t *rows = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + round_up(T * 4));
   engram_status st = engram_compress(token_ids, T, tid2eid, vocab, n_eids, eids, status, stream);

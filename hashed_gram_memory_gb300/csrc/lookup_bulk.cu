@@ -25,6 +25,7 @@
 #include <atomic>
 
 #include "engram_internal.cuh"
+#include "hash_device.cuh"
 #include "lookup_common.cuh"
 
 namespace engram {
@@ -95,9 +96,11 @@ __device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns) {
 // EARLY: the stream slices are loaded into registers before the rows arrive
 // (two blocks per SM); otherwise after them, keeping the block within 64
 // registers per thread so that four blocks share an SM (small tokens).
+// Token t of a one-token-a-block launch, its 3H row ids at `ids` (global or
+// shared memory).
 template <int DT, bool AUX, bool EARLY>
-__global__ void __launch_bounds__(256, EARLY ? 2 : 4)
-    lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
+__device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t *ids,
+                                           const int64_t t) {
   constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;                // FP8 bytes
   constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
   constexpr int kElt = kFp8 ? 1 : 2;
@@ -113,9 +116,7 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   float *s_red = s_scale + kMaxRows;                             // [8][3]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t t = blockIdx.x;
   const int col0 = tid * 16;
-  const int32_t *ids = p.row_ids + t * R;
 
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -265,6 +266,66 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
         mo[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
     }
   }
+}
+
+template <int DT, bool AUX, bool EARLY>
+__global__ void __launch_bounds__(256, EARLY ? 2 : 4)
+    lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
+  const int64_t t = blockIdx.x;
+  bulk_token<DT, AUX, EARLY>(p, p.row_ids + t * 3 * p.H, t);
+}
+
+// The decode step in one launch (one new token per slot, one slot a block):
+// thread 0 compresses the slot's token id, builds its window from the slot's
+// history (the pad id 0 without one), and writes the updated history; the
+// first 3H threads hash the window into the row ids (the hash kernel's
+// arithmetic, hash_device.cuh), kept in shared memory; then the block looks
+// them up as bulk_token does.  A bad token id, map value or history id flags
+// the status word and leaves all of the slot's outputs unwritten.
+template <int DT, bool AUX, bool EARLY>
+__global__ void __launch_bounds__(256, EARLY ? 2 : 4)
+    decode_step_kernel(const __grid_constant__ DecodeParams p) {
+  __shared__ int32_t s_ids[kMaxRows];
+  __shared__ int32_t s_win[4];
+  __shared__ int s_skip;
+  const int64_t b = blockIdx.x;
+  const int H = p.lk.H, R = 3 * H;
+  if (threadIdx.x == 0) {
+    int32_t raw[3] = {0, 0, 0};
+    if (p.history)
+      for (int k = 0; k < 3; ++k) raw[k] = p.history[b * 3 + k];
+    const int32_t tok = p.token_ids[b];
+    uint32_t flag = 0;
+    int32_t e = 0, w[4];
+    if ((uint32_t)tok >= (uint32_t)p.vocab) {
+      flag = ENGRAM_FLAG_BAD_TOKEN;
+    } else {
+      e = __ldg(p.tid2eid + tok);
+      if (e < 0 || e > p.n_eids) flag = ENGRAM_FLAG_BAD_EID;
+    }
+    if (!flag && !make_window(raw, e, p.history ? 3 : 0, w)) flag = ENGRAM_FLAG_BAD_EID;
+    if (!flag) {
+      for (int k = 0; k < 4; ++k) s_win[k] = w[k];
+      if (p.history_out) {
+        p.history_out[b * 3 + 0] = raw[1];
+        p.history_out[b * 3 + 1] = raw[2];
+        p.history_out[b * 3 + 2] = e;
+      }
+    } else if (p.lk.status) {
+      atomicOr(p.lk.status, (int32_t)flag);
+    }
+    s_skip = flag != 0;
+  }
+  __syncthreads();
+  if (s_skip) return;  // block-uniform
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    const int32_t w[4] = {s_win[0], s_win[1], s_win[2], s_win[3]};
+    const int32_t id = window_row(w, r, H, p.seed, p.mod, p.rmul, p.off);
+    s_ids[r] = id;
+    if (p.row_ids_out) p.row_ids_out[b * R + r] = id;
+  }
+  __syncthreads();
+  bulk_token<DT, AUX, EARLY>(p.lk, s_ids, b);
 }
 
 // Small rows (D < 512 with D/16 a power of two, e.g. the released 256-wide
@@ -449,6 +510,38 @@ cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t strea
   return cudaGetLastError();
 }
 
+template <int DT, bool AUX, bool EARLY>
+cudaError_t launch_decode_t(const DecodeParams &p, size_t smem, cudaStream_t stream) {
+  auto kern = decode_step_kernel<DT, AUX, EARLY>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    // the 227 KB a block may use, less this kernel's own static shared memory
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(227 * 1024 - fa.sharedSizeBytes));
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_release);
+  }
+  kern<<<(unsigned)p.lk.T, p.lk.D / 16, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_decode_dt(const DecodeParams &p, size_t smem, bool aux, bool early,
+                             cudaStream_t stream) {
+  if (early)
+    return aux ? launch_decode_t<DT, true, true>(p, smem, stream)
+               : launch_decode_t<DT, false, true>(p, smem, stream);
+  return aux ? launch_decode_t<DT, true, false>(p, smem, stream)
+             : launch_decode_t<DT, false, false>(p, smem, stream);
+}
+
 template <int DT>
 cudaError_t launch_bulk_dt(const LookupParams &p, size_t smem, bool aux, bool early,
                            cudaStream_t stream) {
@@ -533,6 +626,18 @@ size_t bulk_smem_bytes(int D, int dtype, int H) {
 bool bulk_supported(int D, int dtype, int H) {
   return D % 512 == 0 && D >= 512 && D <= ENGRAM_MAX_D &&
          bulk_smem_bytes(D, dtype, H) <= 227 * 1024;
+}
+
+cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream) {
+  if (p.lk.T == 0) return cudaSuccess;
+  const size_t smem = bulk_smem_bytes(p.lk.D, dtype, p.lk.H);
+  const bool aux = p.lk.gate_out != nullptr || p.lk.mem_out != nullptr;
+  const bool early = smem > 56 * 1024;
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
+    return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+    return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32>(p, smem, aux, early, stream);
+  return launch_decode_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream) {

@@ -323,6 +323,12 @@ ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, i
  * `stream`, with the compressed ids and row ids kept in `workspace` (device
  * memory of at least engram_forward_workspace_bytes(batch, seq, n_heads) bytes,
  * 16-byte aligned, owned by the caller, not read after the call's kernels end).
+ * A decode step (seq == 1) whose rows the bulk lookup takes (D a multiple of
+ * 512) runs as one fused launch instead: each slot's block compresses its
+ * token, hashes its window into row ids kept on chip, and looks them up, with
+ * results identical to the three calls; a bad token id, map value or history
+ * id then flags the status word and leaves all of that slot's outputs
+ * (streams, history_out) unwritten.
  *   token_ids int32 [batch, seq] (device); history / history_out as in
  *   engram_hash; streams as in engram_lookup_fused ([batch*seq, 4, D]).
  */

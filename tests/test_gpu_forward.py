@@ -1,5 +1,6 @@
 """The one-call entry points: engram_forward (device buffers) must equal the three
-separate calls bit for bit; engram_forward_host (host ids and streams, chunked
+separate calls bit for bit (for one new token a slot it runs them as one fused
+launch); engram_forward_host (host ids and streams, chunked
 copy/compute pipeline) must equal engram_forward bit for bit, for ragged chunk
 sizes, pinned and pageable host memory, and back-to-back calls that reuse the
 same workspace with different inputs."""
@@ -84,3 +85,71 @@ def test_forward_host_equals_forward(eg, name, chunk, pinned):
     stream.synchronize()
     for (ids_h, x_h, y_h, dev), ref in zip(hosts, outs_dev):
         assert np.array_equal(y_h.numpy().view(np.uint16).reshape(ref.shape), ref)
+
+
+def _decode_case(eg, B=257, H=4, D=4096, rows=(7001, 7013, 7019), with_history=True, seed=5):
+    import torch
+    cfg = W.by_name("decode_fp8").scaled(B=B, H=H, D=D, rows=rows)
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    g = np.random.default_rng(seed)
+    hist = None
+    if with_history:
+        h = inp.history.copy()
+        h[g.choice(B, size=B // 8, replace=False), g.integers(0, 3, size=B // 8)] = -1  # dead
+        hist = torch.from_numpy(h).cuda()
+    return cfg, inp, dev, hist
+
+
+@pytest.mark.parametrize("with_history", [True, False])
+@pytest.mark.parametrize("in_place_history", [False, True])
+def test_fused_decode_equals_three_calls(eg, with_history, in_place_history):
+    """One new token a slot: the fused decode launch gives the streams and the
+    updated history of compress -> hash -> lookup bit for bit, with dead ids in
+    the history (they block the lookback) or no history at all (pad)."""
+    import torch
+    if in_place_history and not with_history:
+        pytest.skip("nothing to update in place")
+    cfg, inp, dev, hist = _decode_case(eg, with_history=with_history)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # the three calls
+    eids = eg.engram_compress(dev["ids"], dev["tid2eid"], cfg.n_eids, status=st)
+    h_sep = torch.empty_like(hist) if hist is not None else None
+    rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=hist, history_out=h_sep, status=st)
+    y_sep = eg.engram_lookup_fused(rows, cfg.H, dev["tables"], dev["streams"], dev["alpha"],
+                                   cfg.eps, status=st)
+    # the fused launch
+    if hist is not None and in_place_history:
+        h_in = hist.clone()
+        h_out = h_in
+    else:
+        h_in, h_out = hist, (torch.empty_like(hist) if hist is not None else None)
+    y = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                          dev["streams"], dev["alpha"], cfg.eps, history=h_in, history_out=h_out,
+                          status=st)
+    assert eg.engram_read_status(st)[1] == 0
+    assert torch.equal(y, y_sep)
+    if hist is not None:
+        assert torch.equal(h_out, h_sep)
+
+
+def test_fused_decode_bad_token_leaves_its_slot_unwritten(eg):
+    """A token id outside the vocabulary flags ENGRAM_FLAG_BAD_TOKEN and leaves
+    that slot's streams and history unwritten; the other slots are exact."""
+    import torch
+    cfg, inp, dev, hist = _decode_case(eg, B=64)
+    ids = dev["ids"].clone()
+    ids[10, 0] = cfg.vocab + 5
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(dev["streams"], 0x1234)
+    h_out = torch.full_like(hist, 77)
+    eg.engram_forward(ids, dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"], dev["streams"],
+                      dev["alpha"], cfg.eps, history=hist, history_out=h_out, streams_out=out,
+                      status=st)
+    assert eg.engram_read_status(st)[1] & eg.FLAG_BAD_TOKEN
+    assert torch.all(out[10] == 0x1234) and torch.all(h_out[10] == 77)
+    good = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                             dev["streams"], dev["alpha"], cfg.eps, history=hist,
+                             history_out=torch.empty_like(hist))
+    keep = [b for b in range(cfg.B) if b != 10]
+    assert torch.equal(out[keep], good[keep])
