@@ -60,42 +60,47 @@ __global__ void __launch_bounds__(256) concat_rows_kernel(const __grid_constant_
     }
     return;
   }
-  // 8 output values (16 bytes of bf16) per step.
-  const int chunks_per_row = d / 8;
+  // 16 output values (two 16-byte words of bf16) per step: one 16-byte load of
+  // FP8 (two of BF16).
+  const int chunks_per_row = d / 16;
   uint4 *erow = reinterpret_cast<uint4 *>(p.e + t * K);
   for (int c = threadIdx.x; c < R * chunks_per_row; c += blockDim.x) {
-    const int r = c / chunks_per_row, col = (c - r * chunks_per_row) * 8;
+    const int r = c / chunks_per_row, col = (c - r * chunks_per_row) * 16;
     const int ni = (r >= H) + (r >= 2 * H);
     const int64_t row = ids[r];
-    uint4 out;
+    uint4 lo, hi;
     if (kBf16) {
-      out = __ldg(reinterpret_cast<const uint4 *>(
-          reinterpret_cast<const uint16_t *>(p.table[ni]) + row * d + col));
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          reinterpret_cast<const uint16_t *>(p.table[ni]) + row * d + col);
+      lo = __ldg(src);
+      hi = __ldg(src + 1);
     } else {
-      const uint2 b = __ldg(reinterpret_cast<const uint2 *>(p.table[ni] + row * d + col));
+      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p.table[ni] + row * d + col));
       const float s = e8m0_to_float(
           __ldg(static_cast<const uint8_t *>(p.scale[ni]) + row * (d >> 5) + (col >> 5)));
-      float f[8];
-      const uint32_t w[2] = {b.x, b.y};
+      float f[16];
+      const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const __half2_raw lo =
+      for (int q = 0; q < 4; ++q) {
+        const __half2_raw l2 =
             __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] & 0xFFFFu), __NV_E4M3);
-        const __half2_raw hi =
-            __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
-        const float2 bb = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-        f[4 * q + 0] = a.x * s;  // a power of two times a 4-bit value: exact, and exact in bf16
+        const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&l2));
+        const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+        // a power of two times a 4-bit value: exact, and exact in bf16 (signed zeros kept)
+        f[4 * q + 0] = a.x * s;
         f[4 * q + 1] = a.y * s;
-        f[4 * q + 2] = bb.x * s;
-        f[4 * q + 3] = bb.y * s;
+        f[4 * q + 2] = c.x * s;
+        f[4 * q + 3] = c.y * s;
       }
-      out.x = pack_bf16(f[0], f[1]);
-      out.y = pack_bf16(f[2], f[3]);
-      out.z = pack_bf16(f[4], f[5]);
-      out.w = pack_bf16(f[6], f[7]);
+      lo = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                      pack_bf16(f[6], f[7]));
+      hi = make_uint4(pack_bf16(f[8], f[9]), pack_bf16(f[10], f[11]), pack_bf16(f[12], f[13]),
+                      pack_bf16(f[14], f[15]));
     }
-    erow[((int64_t)r * d + col) / 8] = out;
+    uint4 *dst = erow + ((int64_t)r * d + col) / 8;
+    dst[0] = lo;
+    dst[1] = hi;
   }
   if (threadIdx.x == 0) p.state[t] = kLive;
 }
