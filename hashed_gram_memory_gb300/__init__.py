@@ -377,8 +377,12 @@ def engram_abi_version() -> int:
 
 
 def engram_set_projection_kernel(which: int) -> int:
-    """PROJECTION_AUTO / PROJECTION_SINGLE / PROJECTION_PAIR; returns the previous choice."""
-    return int(lib.engram_set_projection_kernel(which))
+    """PROJECTION_AUTO / PROJECTION_SINGLE / PROJECTION_PAIR for this process; returns the
+    previous one."""
+    prev = int(lib.engram_set_projection_kernel(which))
+    if prev < 0:
+        raise EngramError(ERR_INVALID_ARG, f"unknown projection kernel {which}")
+    return prev
 
 
 def engram_set_lookup_kernel(which: int) -> int:

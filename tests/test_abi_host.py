@@ -170,6 +170,56 @@ def test_connection_host_argument_errors(eg):
     assert L.engram_gate_add(None, None, 0, 4096, None, None, a, 1e-6, None, None) == OK
 
 
+def test_kernel_selectors(eg):
+    """The lookup and projection selectors take their documented values, return
+    the previous one, and refuse anything else without changing the setting."""
+    for setter, raw, values in ((eg.engram_set_lookup_kernel, eg.lib.engram_set_lookup_kernel,
+                                 (eg.LOOKUP_GATHER, eg.LOOKUP_BULK, eg.LOOKUP_AUTO)),
+                                (eg.engram_set_projection_kernel,
+                                 eg.lib.engram_set_projection_kernel,
+                                 (eg.PROJECTION_SINGLE, eg.PROJECTION_PAIR, eg.PROJECTION_AUTO))):
+        prev = setter(values[0])
+        try:
+            assert setter(values[1]) == values[0]
+            assert raw(7) == -1 and raw(-3) == -1
+            with pytest.raises(eg.EngramError):
+                setter(9)
+            assert setter(values[2]) == values[1]   # unchanged by the refused values
+        finally:
+            setter(prev)
+
+
+def test_forward_decode_host_argument_errors(eg):
+    """engram_forward with one token a slot (the fused decode launch) checks its
+    arguments on the host like the three calls it replaces."""
+    L = eg.lib
+    INV, OK = eg.ERR_INVALID_ARG, eg.OK
+    tok, m, x, y, a = (C.c_void_p(v) for v in (0x4000, 0x8000, 0x100000000, 0x200000000, 0x3000))
+    h = C.c_void_p(0x9000)
+    ws = C.c_void_p(0x300000000)
+    t = _tables(D=4096)
+    need = eg.engram_forward_workspace_bytes(64, 1, 4)
+
+    def fwd(tok=tok, m=m, vocab=100, n_eids=50, hist=h, hist_out=h, x=x, y=y, a=a, eps=1e-6,
+            tb=t, batch=64):
+        return L.engram_forward(tok, batch, 1, m, vocab, n_eids, hist, hist_out, 4,
+                                C.byref(tb) if tb is not None else None, x, y, a, eps, ws, need,
+                                None, None)
+
+    assert fwd(tok=None) == INV
+    assert fwd(m=C.c_void_p(0x8002)) == INV              # map not 4-byte aligned
+    assert fwd(vocab=0) == INV
+    assert fwd(n_eids=-1) == INV
+    assert fwd(hist_out=C.c_void_p(0x9004)) == INV       # partial overlap with history
+    assert fwd(hist_out=C.c_void_p(0x200000010)) == INV  # history_out inside streams_out
+    assert fwd(eps=float("nan")) == INV
+    assert fwd(a=None) == INV
+    assert fwd(y=C.c_void_p(0x100000010)) == INV         # streams overlap partially
+    assert fwd(tb=_tables(D=4096, rows=(10, 0, 10))) == INV
+    assert fwd(tb=None) == INV
+    assert fwd(batch=0) == OK                            # nothing to do
+
+
 def test_python_binding_rejects_cpu_tensors(eg):
     import torch
     with pytest.raises(eg.EngramError):
