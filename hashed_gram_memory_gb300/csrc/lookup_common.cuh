@@ -17,6 +17,17 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// (c0, c1) = fma((a0, a1), (s, s), (c0, c1)) by one packed instruction; each lane
+// rounds exactly as fmaf.
+__device__ __forceinline__ void fma2(float &c0, float &c1, float a0, float a1, float s) {
+  unsigned long long av, sv, cv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(cv) : "f"(c0), "f"(c1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(cv) : "l"(av), "l"(sv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(c0), "=f"(c1) : "l"(cv));
+}
+
 // acc[0..16) += scale * e4m3(v[0..16)); e4m3 -> f16 -> f32 is exact.
 __device__ __forceinline__ void acc_fp8(float (&acc)[16], const uint4 &v, float scale) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -27,10 +38,8 @@ __device__ __forceinline__ void acc_fp8(float (&acc)[16], const uint4 &v, float 
     const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> 16), __NV_E4M3);
     const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
     const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
-    acc[4 * q + 0] = fmaf(a.x, scale, acc[4 * q + 0]);
-    acc[4 * q + 1] = fmaf(a.y, scale, acc[4 * q + 1]);
-    acc[4 * q + 2] = fmaf(b.x, scale, acc[4 * q + 2]);
-    acc[4 * q + 3] = fmaf(b.y, scale, acc[4 * q + 3]);
+    fma2(acc[4 * q + 0], acc[4 * q + 1], a.x, a.y, scale);
+    fma2(acc[4 * q + 2], acc[4 * q + 3], b.x, b.y, scale);
   }
 }
 
