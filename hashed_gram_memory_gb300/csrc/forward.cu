@@ -101,7 +101,7 @@ engram_status decode_step(const int32_t *token_ids, int32_t batch, const int32_t
   if (e != cudaSuccess)
     return engram::set_error(ENGRAM_ERR_CUDA, "engram_forward decode launch: %s",
                              cudaGetErrorString(e));
-  return ENGRAM_OK;
+  return engram::set_error(ENGRAM_OK, "%s", "");  // success clears the last message
 }
 
 }  // namespace
