@@ -491,21 +491,31 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
-template <int DT, bool AUX, bool EARLY>
-cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
-  auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
-  // The shared-memory ceiling is raised once per device to the largest any
-  // launch asks for (227 KB), not at every launch.
-  static std::atomic<uint64_t> configured{0};
+// Raises a kernel's dynamic shared-memory ceiling, once per device, to the 227 KB
+// a block may use less the kernel's static shared memory (any launch's request
+// fits under it).  `configured` is the kernel's own bit set of devices done.
+template <typename Kernel>
+cudaError_t raise_smem_ceiling(Kernel kern, std::atomic<uint64_t> &configured) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_release);
-  }
+  if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(227 * 1024 - fa.sharedSizeBytes));
+  if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+template <int DT, bool AUX, bool EARLY>
+cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
+  auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t e = raise_smem_ceiling(kern, configured);
+  if (e != cudaSuccess) return e;
   kern<<<(unsigned)p.T, p.D / 16, smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -514,20 +524,8 @@ template <int DT, bool AUX, bool EARLY>
 cudaError_t launch_decode_t(const DecodeParams &p, size_t smem, cudaStream_t stream) {
   auto kern = decode_step_kernel<DT, AUX, EARLY>;
   static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = raise_smem_ceiling(kern, configured);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    // the 227 KB a block may use, less this kernel's own static shared memory
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(227 * 1024 - fa.sharedSizeBytes));
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_release);
-  }
   kern<<<(unsigned)p.lk.T, p.lk.D / 16, smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -556,15 +554,8 @@ template <int DT, bool AUX>
 cudaError_t launch_small_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
   auto kern = lookup_bulk_small_kernel<DT, AUX>;
   static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = raise_smem_ceiling(kern, configured);
   if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(configured.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    configured.fetch_or(bit, std::memory_order_release);
-  }
   const int64_t blocks = (p.T + p.tpb - 1) / p.tpb;
   kern<<<(unsigned)blocks, p.tpb * p.tpt, smem, stream>>>(p);
   return cudaGetLastError();

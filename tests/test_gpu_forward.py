@@ -87,9 +87,10 @@ def test_forward_host_equals_forward(eg, name, chunk, pinned):
         assert np.array_equal(y_h.numpy().view(np.uint16).reshape(ref.shape), ref)
 
 
-def _decode_case(eg, B=257, H=4, D=4096, rows=(7001, 7013, 7019), with_history=True, seed=5):
+def _decode_case(eg, B=257, H=4, D=4096, rows=(7001, 7013, 7019), with_history=True, seed=5,
+                 dtype=W.FP8):
     import torch
-    cfg = W.by_name("decode_fp8").scaled(B=B, H=H, D=D, rows=rows)
+    cfg = W.by_name("decode_fp8").scaled(B=B, H=H, D=D, rows=rows, dtype=dtype)
     inp = P.host_inputs(cfg)
     dev = P.to_device(inp)
     g = np.random.default_rng(seed)
@@ -101,16 +102,17 @@ def _decode_case(eg, B=257, H=4, D=4096, rows=(7001, 7013, 7019), with_history=T
     return cfg, inp, dev, hist
 
 
-@pytest.mark.parametrize("with_history", [True, False])
-@pytest.mark.parametrize("in_place_history", [False, True])
-def test_fused_decode_equals_three_calls(eg, with_history, in_place_history):
+@pytest.mark.parametrize("B,dtype,with_history,in_place_history", [
+    (257, W.FP8, True, False), (257, W.FP8, False, False), (257, W.FP8, True, True),
+    (257, W.BF16, True, False), (257, W.FP8_E8M0, True, False),
+    (1500, W.FP8, True, False), (5000, W.FP8_E8M0, True, False)])
+def test_fused_decode_equals_three_calls(eg, B, dtype, with_history, in_place_history):
     """One new token a slot: the fused decode launch gives the streams and the
     updated history of compress -> hash -> lookup bit for bit, with dead ids in
-    the history (they block the lookback) or no history at all (pad)."""
+    the history (they block the lookback) or no history at all (pad), for every
+    table type, and for small and large batches."""
     import torch
-    if in_place_history and not with_history:
-        pytest.skip("nothing to update in place")
-    cfg, inp, dev, hist = _decode_case(eg, with_history=with_history)
+    cfg, inp, dev, hist = _decode_case(eg, B=B, with_history=with_history, dtype=dtype)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     # the three calls
     eids = eg.engram_compress(dev["ids"], dev["tid2eid"], cfg.n_eids, status=st)
