@@ -274,8 +274,8 @@ class Step:
         self.launches = 3
         # One new token a slot: the one-call engram_forward, which runs the decode
         # step as one fused launch (compress, window, hash and lookup).
-        self.fused_decode = (cfg.S == 1 and not cfg.packed and not cfg.hidden and
-                             cfg.D % 512 == 0 and args_lookup_kernel() != "gather")
+        self.fused_decode = (cfg.S == 1 and not cfg.hidden and cfg.D % 512 == 0 and
+                             args_lookup_kernel() != "gather")
         if self.fused_decode:
             self.ws = torch.empty(max(16, eg.engram_forward_workspace_bytes(cfg.B, cfg.S, cfg.H)),
                                   dtype=torch.uint8, device=dev)
@@ -297,7 +297,8 @@ class Step:
             eg.engram_forward(ids, d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], x, d["alpha"],
                               cfg.eps, history=d["history"], history_out=self.hist_out,
                               streams_out=out, workspace=self.ws, status=self.status,
-                              stream=self.stream)
+                              stream=self.stream, positions=d["positions"], dead=d["dead"],
+                              primes=self.primes)
             if ev_end is not None:
                 ev_end.record(self.stream)
             return
@@ -424,8 +425,7 @@ def run_native(args):
     if clocks:
         clocks.stop()
 
-    # engram_forward_host takes no dead mask or positions: no e2e leg for packed batches
-    if args.no_e2e or cfg.packed:
+    if args.no_e2e:
         e2e = None
     elif cfg.hidden:
         e2e = run_e2e_connection(eg, cfg, step, stream, args.e2e_steps, world, device)
@@ -534,26 +534,44 @@ def timed_rounds(one, stream, steps, device):
     return statistics.median(rounds), rounds
 
 
+def host_inputs_pinned(step):
+    """Pinned host copies of a step's per-token inputs: token ids, streams, and
+    the packed layout's positions and dead mask when the workload has them;
+    plus a pinned output buffer and the input bytes they hold."""
+    import torch
+    d = step.d
+
+    def pin(t):
+        return None if t is None else t.cpu().pin_memory()
+
+    h = dict(ids=pin(d["ids"]), positions=pin(d["positions"]), dead=pin(d["dead"]))
+    h["x"] = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    h["x"].copy_(d["streams"])
+    h["y"] = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    h["h2d"] = sum(t.numel() * t.element_size() for k, t in h.items()
+                   if k in ("ids", "positions", "dead", "x") and t is not None)
+    h["d2h"] = h["y"].numel() * h["y"].element_size()
+    return h
+
+
 def run_e2e(eg, cfg, step, stream, steps, world, device):
     """Same metric through the C ABI with HOST buffers: every step is one
-    engram_forward_host call that copies the token ids and the four input streams
-    from pinned host memory, runs compress + hash + the fused lookup, and copies
-    the updated streams back (chunked, copies overlapped with the lookup), all
-    inside the timed region."""
+    engram_forward_host call that copies the token ids (with the packed layout's
+    positions and dead mask) and the four input streams from pinned host memory,
+    runs compress + hash + the fused lookup, and copies the updated streams back
+    (chunked, copies overlapped with the lookup), all inside the timed region."""
     import torch
-    from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
+    from hashed_gram_memory_gb300.replicas import whole_job_throughput
     d = step.d
-    ids_h = d["ids"].cpu().pin_memory()
-    x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
-    x_h.copy_(d["streams"])
-    y_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
+    h = host_inputs_pinned(step)
     ws = torch.empty(eg.engram_forward_host_workspace_bytes(cfg.B, cfg.S, cfg.H, cfg.D, 0),
                      dtype=torch.uint8, device=device)
 
     def one():
-        eg.engram_forward_host(ids_h, d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], x_h, y_h,
-                               d["alpha"], ws, cfg.eps, history=d["history"],
-                               history_out=step.hist_out, status=step.status, stream=stream)
+        eg.engram_forward_host(h["ids"], d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], h["x"],
+                               h["y"], d["alpha"], ws, cfg.eps, history=d["history"],
+                               history_out=step.hist_out, status=step.status, stream=stream,
+                               positions=h["positions"], dead=h["dead"], primes=step.primes)
 
     for _ in range(2):
         one()
@@ -562,41 +580,37 @@ def run_e2e(eg, cfg, step, stream, steps, world, device):
         import torch.distributed as dist
         dist.barrier()
     dt, rounds = timed_rounds(one, stream, steps, device)
-    ok = torch.equal(y_h.to(device), step.out)   # same result as the device-resident step
-    h2d = ids_h.numel() * 4 + x_h.numel() * 2
-    d2h = y_h.numel() * 2
+    ok = torch.equal(h["y"].to(device), step.out)   # same result as the device-resident step
     return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_bytes_per_step": h["h2d"], "d2h_bytes_per_step": h["d2h"], "steps": steps,
             "rounds_tokens_per_s": [whole_job_throughput(world * cfg.T * steps, r) for r in rounds],
             "matches_device_step": bool(ok),
-            "how": "engram_forward_host: pinned host ids + streams in, compress/hash/lookup, "
-                   "streams out; 2048-token chunks, copies overlapped with the lookup on two "
-                   "copy streams; host timer around the steps + a final stream sync; the "
-                   "median of three rounds"}
+            "how": "engram_forward_host: pinned host ids (+ positions, dead mask) + streams in, "
+                   "compress/hash/lookup, streams out; 2048-token chunks, copies overlapped with "
+                   "the lookup on two copy streams; host timer around the steps + a final stream "
+                   "sync; the median of three rounds"}
 
 
 def run_e2e_connection(eg, cfg, step, stream, steps, world, device):
-    """The connection through the public API with HOST buffers: every step copies
-    the token ids and the four input streams from pinned host memory to the
-    device, runs compress, hash and the connection's three calls, and copies the
-    updated streams back to pinned host memory, all inside the timed region."""
+    """The connection through the public API with HOST buffers: every step is one
+    engram_connection_host call that copies the token ids and the four input
+    streams from pinned host memory, runs compress and hash, then the
+    connection (concat, projection, gate + add) chunk by chunk between the
+    copies of its streams in and out, all inside the timed region."""
     import torch
-    from hashed_gram_memory_gb300.replicas import max_over_ranks, whole_job_throughput
+    from hashed_gram_memory_gb300.replicas import whole_job_throughput
     d = step.d
-    ids_h = d["ids"].cpu().pin_memory()
-    x_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
-    x_h.copy_(d["streams"])
-    y_h = torch.empty(d["streams"].shape, dtype=d["streams"].dtype, pin_memory=True)
-    ids_d = torch.empty_like(d["ids"])
-    x_d = torch.empty_like(d["streams"])
-    y_d = torch.empty_like(d["streams"])
+    h = host_inputs_pinned(step)
+    ws = torch.empty(eg.engram_connection_host_workspace_bytes(cfg.B, cfg.S, cfg.H, cfg.D,
+                                                               cfg.hidden, 0),
+                     dtype=torch.uint8, device=device)
 
     def one():
-        with torch.cuda.stream(stream):
-            ids_d.copy_(ids_h, non_blocking=True)
-            x_d.copy_(x_h, non_blocking=True)
-            step(ids=ids_d, x=x_d, out=y_d)
-            y_h.copy_(y_d, non_blocking=True)
+        eg.engram_connection_host(h["ids"], d["tid2eid"], cfg.n_eids, cfg.H, d["tables"],
+                                  d["wkv"], h["x"], h["y"], d["alpha"], ws, cfg.eps,
+                                  history=d["history"], history_out=step.hist_out,
+                                  status=step.status, stream=stream, positions=h["positions"],
+                                  dead=h["dead"], primes=step.primes)
 
     for _ in range(2):
         one()
@@ -605,16 +619,15 @@ def run_e2e_connection(eg, cfg, step, stream, steps, world, device):
         import torch.distributed as dist
         dist.barrier()
     dt, rounds = timed_rounds(one, stream, steps, device)
-    ok = torch.equal(y_h.to(device), step.out)
-    h2d = ids_h.numel() * 4 + x_h.numel() * 2
-    d2h = y_h.numel() * 2
+    ok = torch.equal(h["y"].to(device), step.out)
     return {"value": whole_job_throughput(world * cfg.T * steps, dt), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "h2d_bytes_per_step": h["h2d"], "d2h_bytes_per_step": h["d2h"], "steps": steps,
             "rounds_tokens_per_s": [whole_job_throughput(world * cfg.T * steps, r) for r in rounds],
             "matches_device_step": bool(ok),
-            "how": "pinned host ids + streams copied in, compress / hash / concat / projection / "
-                   "gate + add, streams copied out, one stream, not overlapped; host timer "
-                   "around the steps + a final stream sync; the median of three rounds"}
+            "how": "engram_connection_host: pinned host ids + streams in, compress / hash, then "
+                   "concat / projection / gate + add in 8192-token chunks between the copies of "
+                   "their streams in and out (two copy streams, overlapped); host timer around "
+                   "the steps + a final stream sync; the median of three rounds"}
 
 
 # ----------------------------------------------------------------- CPU oracle

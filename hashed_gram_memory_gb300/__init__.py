@@ -36,6 +36,42 @@ class engram_tables(C.Structure):
                 ("table", C.c_void_p * 3), ("scale", C.c_void_p * 3)]
 
 
+class engram_layout(C.Structure):
+    _fields_ = [("positions", C.c_void_p), ("dead", C.c_void_p),
+                ("primes", C.POINTER(C.c_int64))]
+
+
+def _layout(positions, dead, primes, host: bool):
+    """The engram_layout struct for the whole-path calls (None when all three are
+    None).  positions / dead are device tensors, or host tensors when `host`;
+    primes is [3][n_heads] bucket sizes (host ints).  The struct keeps the
+    primes array alive."""
+    import torch
+    if positions is None and dead is None and primes is None:
+        return None
+    for t, name, dts in ((positions, "positions", (torch.int32,)),
+                         (dead, "dead", (torch.uint8, torch.bool))):
+        if t is None:
+            continue
+        if t.is_cuda == host:
+            where = "host" if host else "CUDA"
+            raise EngramError(ERR_INVALID_ARG, f"{name} must be a {where} tensor here")
+        if t.dtype not in dts or not t.is_contiguous():
+            raise EngramError(ERR_INVALID_ARG, f"{name} must be contiguous {dts}")
+    lay = engram_layout()
+    lay.positions = None if positions is None else positions.data_ptr()
+    lay.dead = None if dead is None else dead.data_ptr()
+    if primes is not None:
+        flat = [int(v) for order in primes for v in order]
+        lay._primes = (C.c_int64 * len(flat))(*flat)
+        lay.primes = C.cast(lay._primes, C.POINTER(C.c_int64))
+    return lay
+
+
+def _ref(lay):
+    return None if lay is None else C.byref(lay)
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -74,18 +110,23 @@ def _load():
     sz = C.c_size_t
     L.engram_forward_workspace_bytes.argtypes = [i32, i32, i32]
     L.engram_forward_workspace_bytes.restype = sz
-    L.engram_forward.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, C.POINTER(engram_tables),
+    tabp, layp = C.POINTER(engram_tables), C.POINTER(engram_layout)
+    L.engram_forward.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, tabp, layp,
                                  vp, vp, vp, C.c_float, vp, sz, vp, vp]
     L.engram_forward.restype = i32
     L.engram_forward_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     L.engram_forward_host_workspace_bytes.restype = sz
-    L.engram_forward_host.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
-                                      C.POINTER(engram_tables), vp, vp, vp, C.c_float, i32, vp, sz,
-                                      vp, vp]
+    L.engram_forward_host.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, tabp, layp,
+                                      vp, vp, vp, C.c_float, i32, vp, sz, vp, vp]
     L.engram_forward_host.restype = i32
-    L.engram_forward_static.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
-                                        C.POINTER(engram_tables), vp, vp, vp, C.c_float, vp, vp]
+    L.engram_forward_static.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, tabp, layp,
+                                        vp, vp, vp, C.c_float, vp, vp]
     L.engram_forward_static.restype = i32
+    L.engram_connection_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.engram_connection_host_workspace_bytes.restype = sz
+    L.engram_connection_host.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, tabp, layp,
+                                         vp, i32, vp, vp, vp, C.c_float, i32, vp, sz, vp, vp]
+    L.engram_connection_host.restype = i32
     L.engram_connection_workspace_bytes.argtypes = [i64, i32, i32, i32]
     L.engram_connection_workspace_bytes.restype = sz
     L.engram_connection.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, i32, vp, vp, vp,
@@ -407,8 +448,11 @@ def engram_forward_workspace_bytes(batch: int, seq: int, n_heads: int) -> int:
 
 def engram_forward(token_ids, tid2eid, n_eids: int, n_heads: int, tables: Tables, streams_in,
                    alpha, eps: float = 1e-6, history=None, history_out=None, streams_out=None,
-                   workspace=None, status=None, stream=None):
-    """compress -> hash -> fused lookup in one call on device tensors; token_ids [B, S]."""
+                   workspace=None, status=None, stream=None, positions=None, dead=None,
+                   primes=None):
+    """compress -> hash -> fused lookup in one call on device tensors; token_ids [B, S].
+    positions [B, S] int32 and dead [B, S] uint8 (device) describe a packed batch;
+    primes ([3][n_heads] bucket sizes) selects the prime-bucket table layout."""
     import torch
     _need(token_ids, (torch.int32,), "token_ids")
     B, S = token_ids.shape
@@ -418,8 +462,9 @@ def engram_forward(token_ids, tid2eid, n_eids: int, n_heads: int, tables: Tables
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=token_ids.device)
     s = tables.struct()
+    lay = _layout(positions, dead, primes, host=False)
     _check(lib.engram_forward(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
-                              _ptr(history), _ptr(history_out), n_heads, C.byref(s),
+                              _ptr(history), _ptr(history_out), n_heads, C.byref(s), _ref(lay),
                               _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
                               _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)),
            "engram_forward")
@@ -434,18 +479,48 @@ def engram_forward_host_workspace_bytes(batch: int, seq: int, n_heads: int, D: i
 def engram_forward_host(token_ids_host, tid2eid, n_eids: int, n_heads: int, tables: Tables,
                         streams_in_host, streams_out_host, alpha, workspace, eps: float = 1e-6,
                         history=None, history_out=None, chunk_tokens: int = 0, status=None,
-                        stream=None):
+                        stream=None, positions=None, dead=None, primes=None):
     """The whole path with host (CPU, ideally pinned) token ids [B, S] and streams
-    [B*S, 4, D]; workspace is a device uint8 tensor of
-    engram_forward_host_workspace_bytes(...) bytes.  Asynchronous on `stream`."""
+    [B*S, 4, D]; positions / dead, when given, are host tensors too.  workspace is
+    a device uint8 tensor of engram_forward_host_workspace_bytes(...) bytes.
+    Asynchronous on `stream`."""
     B, S = token_ids_host.shape
     s = tables.struct()
+    lay = _layout(positions, dead, primes, host=True)
     _check(lib.engram_forward_host(_ptr(token_ids_host), B, S, _ptr(tid2eid), tid2eid.numel(),
                                    n_eids, _ptr(history), _ptr(history_out), n_heads, C.byref(s),
-                                   _ptr(streams_in_host), _ptr(streams_out_host), _ptr(alpha),
+                                   _ref(lay), _ptr(streams_in_host), _ptr(streams_out_host), _ptr(alpha),
                                    float(eps), chunk_tokens, _ptr(workspace), workspace.numel(),
                                    _ptr(status), _stream(stream)),
            "engram_forward_host")
+    return streams_out_host
+
+
+def engram_connection_host_workspace_bytes(batch: int, seq: int, n_heads: int, d: int, D: int,
+                                           chunk_tokens: int = 0) -> int:
+    return int(lib.engram_connection_host_workspace_bytes(batch, seq, n_heads, d, D, chunk_tokens))
+
+
+def engram_connection_host(token_ids_host, tid2eid, n_eids: int, n_heads: int, tables: Tables,
+                           wkv, streams_in_host, streams_out_host, alpha, workspace,
+                           eps: float = 1e-6, history=None, history_out=None,
+                           chunk_tokens: int = 0, status=None, stream=None, positions=None,
+                           dead=None, primes=None):
+    """The connection's whole path with host (ideally pinned) token ids [B, S] and
+    streams [B*S, 4, D] (positions / dead host tensors too); wkv bf16 [D,
+    3*n_heads*d] on the device; workspace a device uint8 tensor of
+    engram_connection_host_workspace_bytes(...) bytes.  Asynchronous on `stream`."""
+    B, S = token_ids_host.shape
+    D = int(wkv.shape[0])
+    s = tables.struct()
+    lay = _layout(positions, dead, primes, host=True)
+    _check(lib.engram_connection_host(_ptr(token_ids_host), B, S, _ptr(tid2eid), tid2eid.numel(),
+                                      n_eids, _ptr(history), _ptr(history_out), n_heads,
+                                      C.byref(s), _ref(lay), _ptr(wkv), D, _ptr(streams_in_host),
+                                      _ptr(streams_out_host), _ptr(alpha), float(eps),
+                                      chunk_tokens, _ptr(workspace), workspace.numel(),
+                                      _ptr(status), _stream(stream)),
+           "engram_connection_host")
     return streams_out_host
 
 
@@ -454,7 +529,8 @@ STATIC_WORKSPACE_BYTES = 16 << 20
 
 def engram_forward_static(token_ids, tid2eid, n_eids: int, n_heads: int, tables: Tables,
                           streams_in, alpha, eps: float = 1e-6, history=None, history_out=None,
-                          streams_out=None, status=None, stream=None):
+                          streams_out=None, status=None, stream=None, positions=None, dead=None,
+                          primes=None):
     """engram_forward without a workspace: the library's fixed device array holds
     the ids (for callers that must not allocate device memory; see engram.h)."""
     import torch
@@ -463,9 +539,10 @@ def engram_forward_static(token_ids, tid2eid, n_eids: int, n_heads: int, tables:
     if streams_out is None:
         streams_out = torch.empty_like(streams_in)
     s = tables.struct()
+    lay = _layout(positions, dead, primes, host=False)
     _check(lib.engram_forward_static(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
                                      _ptr(history), _ptr(history_out), n_heads, C.byref(s),
-                                     _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
+                                     _ref(lay), _ptr(streams_in), _ptr(streams_out), _ptr(alpha), float(eps),
                                      _ptr(status), _stream(stream)),
            "engram_forward_static")
     return streams_out

@@ -71,6 +71,8 @@ struct DecodeParams {
   const int32_t *history;    // [batch, 3] oldest first, or NULL (pad)
   int32_t *history_out;      // [batch, 3] or NULL; may be history
   int32_t *row_ids_out;      // [batch, 3H] or NULL
+  const int32_t *positions;  // [batch] or NULL: the token's index within its sample
+  const uint8_t *dead;       // [batch] or NULL: dead slots (every id ENGRAM_ROW_DEAD)
   int32_t vocab, n_eids;
   uint64_t mod[3][kMaxHeads];
   uint64_t off[3][kMaxHeads];

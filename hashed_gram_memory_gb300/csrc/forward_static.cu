@@ -25,8 +25,9 @@ extern "C" {
 ENGRAM_API engram_status engram_forward_static(
     const int32_t *token_ids, int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
     int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
-    const engram_tables *tables_host, const uint16_t *streams_in, uint16_t *streams_out,
-    const float *alpha, float eps, int32_t *status, void *stream) {
+    const engram_tables *tables_host, const engram_layout *layout_host,
+    const uint16_t *streams_in, uint16_t *streams_out, const float *alpha, float eps,
+    int32_t *status, void *stream) {
   if (batch < 0 || seq < 0 || n_heads < 1 || n_heads > ENGRAM_MAX_HEADS || !tables_host)
     return engram::set_error(ENGRAM_ERR_INVALID_ARG, "engram_forward_static: bad sizes or NULL tables");
   const size_t need = engram_forward_workspace_bytes(batch, seq, n_heads);
@@ -67,7 +68,7 @@ ENGRAM_API engram_status engram_forward_static(
                                cudaGetErrorString(e));
   }
   return engram_forward(token_ids, batch, seq, tid2eid, vocab, n_eids, history, history_out,
-                        n_heads, tables_host, streams_in, streams_out, alpha, eps, ws,
+                        n_heads, tables_host, layout_host, streams_in, streams_out, alpha, eps, ws,
                         (size_t)ENGRAM_STATIC_WORKSPACE_BYTES, status, stream);
 }
 

@@ -276,10 +276,12 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
 }
 
 // The decode step in one launch (one new token per slot, one slot a block):
-// thread 0 compresses the slot's token id, builds its window from the slot's
-// history (the pad id 0 without one), and writes the updated history; the
-// first 3H threads hash the window into the row ids (the hash kernel's
-// arithmetic, hash_device.cuh), kept in shared memory; then the block looks
+// thread 0 compresses the slot's token id (a slot of the dead mask becomes the
+// dead id), builds its window from the slot's history (the pad id 0 without
+// one) back to its lookback limit (its position in its sample when positions
+// are given), and writes the updated history; the first 3H threads hash the
+// window into the row ids (the hash kernel's arithmetic, hash_device.cuh; a
+// dead slot gets ENGRAM_ROW_DEAD), kept in shared memory; then the block looks
 // them up as bulk_token does.  A bad token id, map value or history id flags
 // the status word and leaves all of the slot's outputs unwritten.
 template <int DT, bool AUX, bool EARLY>
@@ -287,25 +289,32 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
     decode_step_kernel(const __grid_constant__ DecodeParams p) {
   __shared__ int32_t s_ids[kMaxRows];
   __shared__ int32_t s_win[4];
-  __shared__ int s_skip;
+  __shared__ int s_skip, s_dead;
   const int64_t b = blockIdx.x;
   const int H = p.lk.H, R = 3 * H;
   if (threadIdx.x == 0) {
     int32_t raw[3] = {0, 0, 0};
     if (p.history)
       for (int k = 0; k < 3; ++k) raw[k] = p.history[b * 3 + k];
-    const int32_t tok = p.token_ids[b];
+    // A dead slot compresses to the dead id whatever its token (no range check).
+    const bool dead = p.dead && p.dead[b];
     uint32_t flag = 0;
-    int32_t e = 0, w[4];
-    if ((uint32_t)tok >= (uint32_t)p.vocab) {
-      flag = ENGRAM_FLAG_BAD_TOKEN;
-    } else {
-      e = __ldg(p.tid2eid + tok);
-      if (e < 0 || e > p.n_eids) flag = ENGRAM_FLAG_BAD_EID;
+    int32_t e = ENGRAM_EID_DEAD, w[4];
+    if (!dead) {
+      const int32_t tok = p.token_ids[b];
+      if ((uint32_t)tok >= (uint32_t)p.vocab) {
+        flag = ENGRAM_FLAG_BAD_TOKEN;
+      } else {
+        e = __ldg(p.tid2eid + tok);
+        if (e < 0 || e > p.n_eids) flag = ENGRAM_FLAG_BAD_EID;
+      }
+      // lookback: the position in the sample if given, else the 3-id history or nothing
+      const int64_t limit = p.positions ? (int64_t)p.positions[b] : (p.history ? 3 : 0);
+      if (!flag && !make_window(raw, e, limit, w)) flag = ENGRAM_FLAG_BAD_EID;
     }
-    if (!flag && !make_window(raw, e, p.history ? 3 : 0, w)) flag = ENGRAM_FLAG_BAD_EID;
     if (!flag) {
-      for (int k = 0; k < 4; ++k) s_win[k] = w[k];
+      if (!dead)
+        for (int k = 0; k < 4; ++k) s_win[k] = w[k];
       if (p.history_out) {
         p.history_out[b * 3 + 0] = raw[1];
         p.history_out[b * 3 + 1] = raw[2];
@@ -315,12 +324,16 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
       atomicOr(p.lk.status, (int32_t)flag);
     }
     s_skip = flag != 0;
+    s_dead = dead;
   }
   __syncthreads();
   if (s_skip) return;  // block-uniform
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    const int32_t w[4] = {s_win[0], s_win[1], s_win[2], s_win[3]};
-    const int32_t id = window_row(w, r, H, p.seed, p.mod, p.rmul, p.off);
+    int32_t id = ENGRAM_ROW_DEAD;
+    if (!s_dead) {
+      const int32_t w[4] = {s_win[0], s_win[1], s_win[2], s_win[3]};
+      id = window_row(w, r, H, p.seed, p.mod, p.rmul, p.off);
+    }
     s_ids[r] = id;
     if (p.row_ids_out) p.row_ids_out[b * R + r] = id;
   }

@@ -318,11 +318,36 @@ ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, i
                                          float *gate_out, void *stream);
 
 /*
+ * engram_layout -- how a batch is packed and how the tables are cut, for the
+ * whole-path calls below.  A NULL struct, or NULL members, mean the plain case:
+ * every sequence is one sample from position 0, nothing is dead, and order n
+ * has its own table of tables_host->rows[n-2] rows.
+ *   positions  int32 [batch, seq]: each token's index within its own sample,
+ *              as for engram_hash_packed (VeOmni PR page, review of
+ *              pack_ngram_inputs: no n-gram crosses a sample boundary)
+ *   dead       uint8 [batch*seq]: non-zero marks a dead token, as for
+ *              engram_compress_masked
+ *   primes     HOST int64 [3*n_heads]: one table cut into prime buckets, as
+ *              for engram_hash_bucketed (the released layout); tables_host
+ *              then names that one table for all three orders, and the
+ *              buckets' sum must be at most each of its rows[n]
+ * positions and dead are device memory for engram_forward and
+ * engram_forward_static, host memory (like the token ids) for the *_host
+ * calls.  The struct itself is read on the host during the call only.
+ */
+typedef struct engram_layout {
+  const int32_t *positions;
+  const uint8_t *dead;
+  const int64_t *primes;
+} engram_layout;
+
+/*
  * engram_forward -- the whole path in one call on device buffers:
- * engram_compress, engram_hash and engram_lookup_fused back to back on
- * `stream`, with the compressed ids and row ids kept in `workspace` (device
- * memory of at least engram_forward_workspace_bytes(batch, seq, n_heads) bytes,
- * 16-byte aligned, owned by the caller, not read after the call's kernels end).
+ * engram_compress_masked, engram_hash_packed (or engram_hash_bucketed) and
+ * engram_lookup_fused back to back on `stream`, with the compressed ids and
+ * row ids kept in `workspace` (device memory of at least
+ * engram_forward_workspace_bytes(batch, seq, n_heads) bytes, 16-byte aligned,
+ * owned by the caller, not read after the call's kernels end).
  * A decode step (seq == 1) whose rows the bulk lookup takes (D a multiple of
  * 512) runs as one fused launch instead: each slot's block compresses its
  * token, hashes its window into row ids kept on chip, and looks them up, with
@@ -330,21 +355,24 @@ ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, i
  * id then flags the status word and leaves all of that slot's outputs
  * (streams, history_out) unwritten.
  *   token_ids int32 [batch, seq] (device); history / history_out as in
- *   engram_hash; streams as in engram_lookup_fused ([batch*seq, 4, D]).
+ *   engram_hash; layout_host as above (may be NULL); streams as in
+ *   engram_lookup_fused ([batch*seq, 4, D]).
  */
 ENGRAM_API size_t engram_forward_workspace_bytes(int32_t batch, int32_t seq, int32_t n_heads);
 ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch, int32_t seq,
                                         const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
                                         const int32_t *history, int32_t *history_out,
                                         int32_t n_heads, const engram_tables *tables_host,
+                                        const engram_layout *layout_host,
                                         const uint16_t *streams_in, uint16_t *streams_out,
                                         const float *alpha, float eps, void *workspace,
                                         size_t workspace_bytes, int32_t *status, void *stream);
 
 /*
- * engram_forward_host -- the whole path with the token ids and the streams in
- * HOST memory (pinned for overlap; pageable works but serialises the copies).
- * The call copies the ids in, runs compress + hash, then pipelines the streams
+ * engram_forward_host -- the whole path with the token ids, the layout's
+ * positions and dead mask, and the streams in HOST memory (pinned for overlap;
+ * pageable works but serialises the copies).  The call copies the ids (and
+ * positions, dead mask) in, runs compress + hash, then pipelines the streams
  * in chunks of `chunk_tokens` tokens (0 = 2048): host->device copies on one
  * internal copy stream, the fused lookup on `stream`, device->host copies on a
  * second copy stream, with three chunk buffers per direction in `workspace`
@@ -352,8 +380,9 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
  * Returns once everything is enqueued; `stream` is ordered after the last
  * device->host copy, so synchronising `stream` means streams_out_host is final.
  * The two copy streams and their events are created on first use per device
- * and kept for the life of the process.  tid2eid, history, history_out, the
- * tables, alpha and status are device memory as in the calls above.
+ * and kept for the life of the process; calls on one device take turns on
+ * them.  tid2eid, history, history_out, the tables, alpha and status are device
+ * memory as in the calls above.
  */
 ENGRAM_API size_t engram_forward_host_workspace_bytes(int32_t batch, int32_t seq,
                                                       int32_t n_heads, int32_t D,
@@ -361,9 +390,34 @@ ENGRAM_API size_t engram_forward_host_workspace_bytes(int32_t batch, int32_t seq
 ENGRAM_API engram_status engram_forward_host(
     const int32_t *token_ids_host, int32_t batch, int32_t seq, const int32_t *tid2eid,
     int32_t vocab, int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
-    const engram_tables *tables_host, const uint16_t *streams_in_host,
-    uint16_t *streams_out_host, const float *alpha, float eps, int32_t chunk_tokens,
-    void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+    const engram_tables *tables_host, const engram_layout *layout_host,
+    const uint16_t *streams_in_host, uint16_t *streams_out_host, const float *alpha, float eps,
+    int32_t chunk_tokens, void *workspace, size_t workspace_bytes, int32_t *status, void *stream);
+
+/*
+ * engram_connection_host -- the connection's whole path (engram_compress_masked,
+ * the hash, then engram_connection) with the token ids, the layout's positions
+ * and dead mask, and the streams in HOST memory, pipelined as
+ * engram_forward_host does: the ids are copied in and hashed on `stream`, then
+ * the streams move in chunks of `chunk_tokens` tokens (0 = 8192, enough
+ * 256-row projection tiles to fill every SM pair), each chunk's connection (rows
+ * into E, k = wkv e on the tensor cores, gate and add) running on `stream`
+ * between its two copies.  D is the stream width (wkv is bf16 [D, 3*n_heads*d],
+ * d = tables_host->D); tables and wkv as for engram_connection.  workspace:
+ * device, 256-byte aligned, at least engram_connection_host_workspace_bytes(...)
+ * bytes.  Returns once everything is enqueued; synchronising `stream` means
+ * streams_out_host is final.  It shares engram_forward_host's copy streams.
+ */
+ENGRAM_API size_t engram_connection_host_workspace_bytes(int32_t batch, int32_t seq,
+                                                         int32_t n_heads, int32_t d, int32_t D,
+                                                         int32_t chunk_tokens);
+ENGRAM_API engram_status engram_connection_host(
+    const int32_t *token_ids_host, int32_t batch, int32_t seq, const int32_t *tid2eid,
+    int32_t vocab, int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
+    const engram_tables *tables_host, const engram_layout *layout_host, const uint16_t *wkv,
+    int32_t D, const uint16_t *streams_in_host, uint16_t *streams_out_host, const float *alpha,
+    float eps, int32_t chunk_tokens, void *workspace, size_t workspace_bytes, int32_t *status,
+    void *stream);
 
 /*
  * engram_forward_static -- engram_forward without a workspace argument, for
@@ -392,8 +446,9 @@ ENGRAM_API engram_status engram_forward_host(
 ENGRAM_API engram_status engram_forward_static(
     const int32_t *token_ids, int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
     int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
-    const engram_tables *tables_host, const uint16_t *streams_in, uint16_t *streams_out,
-    const float *alpha, float eps, int32_t *status, void *stream);
+    const engram_tables *tables_host, const engram_layout *layout_host,
+    const uint16_t *streams_in, uint16_t *streams_out, const float *alpha, float eps,
+    int32_t *status, void *stream);
 
 /*
  * engram_read_status -- waits for `stream`, copies the device status word into
@@ -465,7 +520,7 @@ ENGRAM_API const char *engram_status_string(engram_status code);
 ENGRAM_API const char *engram_last_error(void);
 
 /* ABI version of this header (incremented on any incompatible change). */
-#define ENGRAM_ABI_VERSION 3
+#define ENGRAM_ABI_VERSION 4
 ENGRAM_API int32_t engram_abi_version(void);
 
 #ifdef __cplusplus

@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol(eg):
 
 
 def test_abi_version_and_strings(eg):
-    assert eg.engram_abi_version() == 3
+    assert eg.engram_abi_version() == 4
     for code in range(6):
         assert eg.engram_status_string(code).startswith("ENGRAM")
     assert "unknown" in eg.engram_status_string(99)
@@ -201,10 +201,19 @@ def test_forward_decode_host_argument_errors(eg):
     need = eg.engram_forward_workspace_bytes(64, 1, 4)
 
     def fwd(tok=tok, m=m, vocab=100, n_eids=50, hist=h, hist_out=h, x=x, y=y, a=a, eps=1e-6,
-            tb=t, batch=64):
+            tb=t, batch=64, lay=None):
         return L.engram_forward(tok, batch, 1, m, vocab, n_eids, hist, hist_out, 4,
-                                C.byref(tb) if tb is not None else None, x, y, a, eps, ws, need,
+                                C.byref(tb) if tb is not None else None,
+                                C.byref(lay) if lay is not None else None, x, y, a, eps, ws, need,
                                 None, None)
+
+    def layout(pos=None, dead=None, primes=None):
+        lay = eg.engram_layout()
+        lay.positions, lay.dead = pos, dead
+        if primes is not None:
+            lay._keep = (C.c_int64 * len(primes))(*primes)
+            lay.primes = C.cast(lay._keep, C.POINTER(C.c_int64))
+        return lay
 
     assert fwd(tok=None) == INV
     assert fwd(m=C.c_void_p(0x8002)) == INV              # map not 4-byte aligned
@@ -217,7 +226,62 @@ def test_forward_decode_host_argument_errors(eg):
     assert fwd(y=C.c_void_p(0x100000010)) == INV         # streams overlap partially
     assert fwd(tb=_tables(D=4096, rows=(10, 0, 10))) == INV
     assert fwd(tb=None) == INV
+    assert fwd(lay=layout(pos=0xA002)) == INV            # positions not 4-byte aligned
+    assert fwd(hist=None, hist_out=C.c_void_p(0xA000), lay=layout(pos=0xA000)) == INV
+    assert fwd(lay=layout(primes=[7] * 11 + [0])) == INV  # a bucket of no rows
+    assert fwd(lay=layout(primes=[11] * 12)) == INV      # 132 bucket rows > the 10-row tables
     assert fwd(batch=0) == OK                            # nothing to do
+    assert fwd(batch=0, tb=_tables(D=4096, rows=(100, 100, 100)),
+               lay=layout(pos=0xA000, dead=0xB000, primes=[7] * 12)) == OK
+
+
+def test_host_buffer_calls_argument_errors(eg):
+    """engram_forward_host and engram_connection_host check their arguments,
+    workspace and layout before creating copy streams or touching a device."""
+    L = eg.lib
+    INV, OK = eg.ERR_INVALID_ARG, eg.OK
+    tok, m, x, y, a = (C.c_void_p(v) for v in (0x4000, 0x8000, 0x100000000, 0x200000000, 0x3000))
+    w = C.c_void_p(0x8000000)
+    t = _tables(D=4096)
+    e8 = _tables(dtype=2, D=256, rows=(100000, 100000, 100000))
+    need_f = eg.engram_forward_host_workspace_bytes(8, 128, 4, 4096, 0)
+    need_c = eg.engram_connection_host_workspace_bytes(8, 128, 8, 256, 4096, 0)
+    # ids, positions, eids, dead, rows, then three chunk buffers each way (+ the connection's)
+    assert need_f == 3 * 4096 + 1024 + 1024 * 12 * 4 + 6 * 2048 * 4 * 4096 * 2
+    assert need_c == (3 * 4096 + 1024 + 1024 * 24 * 4 + 6 * 8192 * 4 * 4096 * 2 +
+                      eg.engram_connection_workspace_bytes(8192, 8, 256, 4096))
+    ws = C.c_void_p(0x300000000)
+
+    def fh(tok=tok, tb=t, work=ws, wb=need_f, chunk=0, xin=x, lay=None):
+        return L.engram_forward_host(tok, 8, 128, m, 100, 50, None, None, 4,
+                                     C.byref(tb) if tb is not None else None,
+                                     C.byref(lay) if lay is not None else None, xin, y, a, 1e-6,
+                                     chunk, work, wb, None, None)
+
+    def ch(tok=tok, tb=e8, work=ws, wb=need_c, chunk=0, xin=x, lay=None, D=4096):
+        return L.engram_connection_host(tok, 8, 128, m, 100, 50, None, None, 8,
+                                        C.byref(tb) if tb is not None else None,
+                                        C.byref(lay) if lay is not None else None, w, D, xin, y,
+                                        a, 1e-6, chunk, work, wb, None, None)
+
+    for call, need in ((fh, need_f), (ch, need_c)):
+        assert call(tok=None) == INV                      # NULL host ids
+        assert call(xin=None) == INV                      # NULL host streams
+        assert call(tb=None) == INV
+        assert call(work=None) == INV
+        assert call(wb=need - 1) == INV                   # short workspace
+        assert call(chunk=-1) == INV
+        bad = eg.engram_layout()
+        bad._keep = (C.c_int64 * 24)(*([0] * 24))
+        bad.primes = C.cast(bad._keep, C.POINTER(C.c_int64))
+        assert call(lay=bad) == INV                       # buckets of no rows
+    assert ch(work=C.c_void_p(0x300000080)) == INV        # not 256-byte aligned
+    assert fh(tb=_tables(D=4100)) == INV                  # row width not a multiple of 16
+    assert ch(D=0) == INV
+    # the lookup's and the connection's own checks run before anything is enqueued
+    assert fh(tb=_tables(dtype=7, D=4096)) == INV         # unknown table type
+    assert ch(tb=_tables(dtype=0, D=256, rows=(100000,) * 3)) == eg.ERR_UNSUPPORTED
+    assert ch(D=4000) == eg.ERR_UNSUPPORTED               # stream width not a multiple of 256
 
 
 def test_python_binding_rejects_cpu_tensors(eg):

@@ -30,16 +30,20 @@ def _p(t):
 def _static_call(eg, cfg, dev, out, status, stream):
     B, S = dev["ids"].shape
     tb = dev["tables"].struct()
+    lay = eg._layout(dev.get("positions"), dev.get("dead"), None, host=False)
     return eg.lib.engram_forward_static(
         _p(dev["ids"]), B, S, _p(dev["tid2eid"]), dev["tid2eid"].numel(), cfg.n_eids,
-        _p(dev["history"]), None, cfg.H, C.byref(tb), _p(dev["streams"]), _p(out),
-        _p(dev["alpha"]), float(cfg.eps), _p(status), C.c_void_p(stream.cuda_stream))
+        _p(dev["history"]), None, cfg.H, C.byref(tb), None if lay is None else C.byref(lay),
+        _p(dev["streams"]), _p(out), _p(dev["alpha"]), float(cfg.eps), _p(status),
+        C.c_void_p(stream.cuda_stream))
 
 
 def test_static_entry_point_matches_forward_on_two_calls(eg):
     import torch
     cases = [W.by_name("full_prefill_fp8").scaled(B=2, S=517, rows=(6007, 6011, 6029)),       # prefill, 8 heads
-             W.by_name("decode_fp8").scaled(B=300, rows=(7001, 7013, 7019))]           # decode with history
+             W.by_name("decode_fp8").scaled(B=300, rows=(7001, 7013, 7019)),           # decode with history
+             W.by_name("packed_mm_fp8").scaled(B=2, S=300, rows=(6007, 6011, 6029),    # packed, dead spans
+                                               mean_sample_len=40, image_span=8, image_frac=0.3)]
     stream = torch.cuda.Stream()
     for i, cfg in enumerate(cases):
         inp = P.host_inputs(cfg, rank=i)
@@ -50,7 +54,8 @@ def test_static_entry_point_matches_forward_on_two_calls(eg):
             code = _static_call(eg, cfg, dev, out, status, stream)
             assert code == eg.OK, eg.lib.engram_last_error()
             ref = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
-                                    dev["streams"], dev["alpha"], cfg.eps, history=dev["history"])
+                                    dev["streams"], dev["alpha"], cfg.eps, history=dev["history"],
+                                    positions=dev["positions"], dead=dev["dead"])
         stream.synchronize()
         assert eg.engram_read_status(status)[1] == 0
         got = out.cpu().numpy().view(np.uint16)
