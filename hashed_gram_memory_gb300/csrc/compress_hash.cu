@@ -42,25 +42,31 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   flag_warp(p.status, flags);
 }
 
-// One thread per (token, order, head).  Thread r of a token computes row id r
-// (n-major: r = (n-2)*H + j) from the token's window, read back from the token
-// until its lookback limit (its position in its sample if positions are given,
-// else 3 with a history and s without) or a dead id, whichever comes first;
-// the slots beyond hold the pad id 0.  A dead token writes ENGRAM_ROW_DEAD.
-__global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashParams p) {
-  const int R = 3 * p.H;
-  const int tl = threadIdx.x / R;
-  const int r = threadIdx.x - tl * R;
-  const int64_t t = (int64_t)blockIdx.x * p.tokens_per_block + tl;
-  const bool valid = tl < p.tokens_per_block && t < p.T;
+// One thread per token.  The thread reads the token's window once, back from
+// the token until its lookback limit (its position in its sample if positions
+// are given, else 3 with a history and s without) or a dead id, whichever comes
+// first (the slots beyond hold the pad id 0), and computes its 3H row ids in a
+// loop whose (order, head) index is the same in every lane: the per-(n, head)
+// seeds, moduli and offsets are then warp-uniform parameter loads (an index
+// that differs between lanes serialises them).  A dead token gets
+// ENGRAM_ROW_DEAD.  The ids are staged in shared memory at an odd stride
+// (conflict-free) and stored by the whole block, so that the stores are
+// contiguous: the block's tokens own one contiguous range of row_ids.
+constexpr int kHashTokens = 64;
+
+__global__ void __launch_bounds__(kHashTokens) hash_kernel(const __grid_constant__ HashParams p) {
+  extern __shared__ int32_t s_rows[];  // [kHashTokens][stride], then [kHashTokens] skip flags
+  const int R = 3 * p.H, stride = R | 1;
+  int32_t *s_skip = s_rows + kHashTokens * stride;
+  const int64_t t0 = (int64_t)blockIdx.x * kHashTokens;
+  const int64_t t = t0 + threadIdx.x;
   uint32_t flags = 0;
-  int32_t w[4] = {0, 0, 0, 0};  // oldest first, w[3] = the token's own id
-  int32_t raw[4] = {0, 0, 0, 0};  // the ids s-3 .. s as stored (for history_out)
-  int b = 0;
-  if (valid) {
-    b = (int)(t / p.seq);
+  int skip = 1;
+  if (t < p.T) {
+    const int b = (int)(t / p.seq);
     const int s = (int)(t - (int64_t)b * p.seq);
     const int64_t base = (int64_t)b * p.seq;
+    int32_t raw[4] = {0, 0, 0, 0};  // the ids s-3 .. s as stored (for history_out)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int pos = s - 3 + k;
@@ -70,28 +76,45 @@ __global__ void __launch_bounds__(256) hash_kernel(const __grid_constant__ HashP
         raw[k] = p.history[(int64_t)b * 3 + 3 + pos];  // plain load: history may be rewritten below
     }
     const int32_t self = raw[3];
-    bool dead = self == ENGRAM_EID_DEAD, bad = self < ENGRAM_EID_DEAD;
+    const bool dead = self == ENGRAM_EID_DEAD;
+    bool bad = self < ENGRAM_EID_DEAD;
+    int32_t w[4] = {0, 0, 0, 0};  // oldest first, w[3] = the token's own id
     if (!dead && !bad) {
       // positions before 0 hold the history or 0 (raw), so the limit alone decides
       const int64_t limit = p.positions ? (int64_t)p.positions[base + s] : (p.history ? 3 : s);
       const int32_t before[3] = {raw[0], raw[1], raw[2]};
       bad = !make_window(before, self, limit, w);
     }
+    int32_t *mine = s_rows + threadIdx.x * stride;
     if (bad) {
       flags = ENGRAM_FLAG_BAD_EID;
     } else if (dead) {
-      p.row_ids[t * R + r] = ENGRAM_ROW_DEAD;
+      for (int r = 0; r < R; ++r) mine[r] = ENGRAM_ROW_DEAD;
     } else {
-      p.row_ids[t * R + r] = window_row(w, r, p.H, p.seed, p.mod, p.rmul, p.off);
+      for (int r = 0; r < R; ++r) mine[r] = window_row(w, r, p.H, p.seed, p.mod, p.rmul, p.off);
     }
-  }
-  flag_warp(p.status, flags);
-  if (p.history_inline) {
-    // seq == 1: every reader of history[b] is a thread of this block.
-    __syncthreads();
-    if (valid && r == 0) {
+    skip = bad;
+    if (p.history_inline) {
+      // seq == 1: this thread is the only reader of history[b], and it is done.
 #pragma unroll
       for (int k = 0; k < 3; ++k) p.history_out[(int64_t)b * 3 + k] = raw[k + 1];
+    }
+  }
+  s_skip[threadIdx.x] = skip;
+  flag_warp(p.status, flags);
+  __syncthreads();
+  // Contiguous stores: element i of the block's range is row r of token tl.
+  const int64_t left = p.T - t0;
+  const int n = left < kHashTokens ? (int)left : kHashTokens;
+  int tl = (int)threadIdx.x / R, r = (int)threadIdx.x - tl * R;
+  const int dq = kHashTokens / R, dr = kHashTokens - dq * R;  // kHashTokens = dq*R + dr
+  for (int i = threadIdx.x; i < n * R; i += kHashTokens) {
+    if (!s_skip[tl]) p.row_ids[t0 * R + i] = s_rows[tl * stride + r];
+    tl += dq;
+    r += dr;
+    if (r >= R) {
+      r -= R;
+      ++tl;
     }
   }
 }
@@ -134,13 +157,13 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t stream) {
 cudaError_t launch_hash(const HashParams &p_in, cudaStream_t stream) {
   HashParams p = p_in;
   const int R = 3 * p.H;
-  p.tokens_per_block = 256 / R > 0 ? 256 / R : 1;
+  p.tokens_per_block = kHashTokens;
   p.history_inline = (p.history_out != nullptr && p.seq == 1) ? 1 : 0;
   if (p.T > 0) {
-    // Whole warps: flag_warp reduces over full warps; padding threads are invalid.
-    const int threads = (p.tokens_per_block * R + 31) / 32 * 32;
-    const int64_t blocks = (p.T + p.tokens_per_block - 1) / p.tokens_per_block;
-    hash_kernel<<<(unsigned)blocks, threads, 0, stream>>>(p);
+    // kHashTokens is whole warps: flag_warp reduces over full warps.
+    const size_t smem = (size_t)kHashTokens * ((R | 1) + 1) * sizeof(int32_t);
+    const int64_t blocks = (p.T + kHashTokens - 1) / kHashTokens;
+    hash_kernel<<<(unsigned)blocks, kHashTokens, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
