@@ -341,6 +341,26 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   bulk_token<DT, AUX, EARLY>(p.lk, s_ids, b);
 }
 
+// A row's e8m0 exponents, n = D/32 bytes with n in {1, 2, 4, 8} (the small-row
+// kernel's widths), as one naturally aligned load and store.
+__device__ __forceinline__ uint64_t load_exps(const uint8_t *e, uint32_t n) {
+  if (n == 8) return __ldg(reinterpret_cast<const unsigned long long *>(e));
+  if (n == 4) return __ldg(reinterpret_cast<const unsigned int *>(e));
+  if (n == 2) return __ldg(reinterpret_cast<const unsigned short *>(e));
+  return __ldg(e);
+}
+
+__device__ __forceinline__ void store_exps(uint8_t *se, uint64_t v, uint32_t n) {
+  if (n == 8)
+    *reinterpret_cast<uint64_t *>(se) = v;
+  else if (n == 4)
+    *reinterpret_cast<uint32_t *>(se) = (uint32_t)v;
+  else if (n == 2)
+    *reinterpret_cast<uint16_t *>(se) = (uint16_t)v;
+  else
+    *se = (uint8_t)v;
+}
+
 // Small rows (D < 512 with D/16 a power of two, e.g. the released 256-wide
 // rows): several tokens per block, each handled by its tpt = D/16 threads, which
 // issue the copies of the token's rows themselves (thread l of the token copies
@@ -412,24 +432,35 @@ __global__ void __launch_bounds__(256, 2)
     mbar_arrive_expect_tx(bar, my_bytes);
   else
     mbar_arrive(bar);
+  // This thread's rows (r = lane_t + k*tpt): the copy, then the load of the
+  // row's scale or exponents (1, 2, 4 or 8 bytes: one load), issued together.
+  // The first four rows' words are stored to shared memory only after the
+  // stream loads are issued (a store waits for its load); further rows' at once.
+  uint64_t v[4] = {0, 0, 0, 0};
+  bool withhold = work && p.withhold != 0 && tid == 0;  // test hook: one copy never issued
+  uint8_t *dst = s_rows + (size_t)tl * tok_bytes;
+  auto issue_row = [&](int r) -> uint64_t {
+    const int ni = (r >= H) + (r >= 2 * H);
+    const int64_t id = ids[r];
+    if (withhold)
+      withhold = false;
+    else
+      bulk_g2s(dst + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
+    if (kE8) return load_exps(static_cast<const uint8_t *>(p.scale[ni]) + id * exp_bytes, exp_bytes);
+    if (kFp8) return __float_as_uint(__ldg(static_cast<const float *>(p.scale[ni]) + id));
+    return 0;
+  };
+  auto store_row = [&](int r, uint64_t w) {
+    if (kE8)
+      store_exps(s_exps + ((size_t)tl * R + r) * exp_bytes, w, exp_bytes);
+    else if (kFp8)
+      s_scale[(size_t)tl * R + r] = __uint_as_float((uint32_t)w);
+  };
   if (work) {
-    bool withhold = p.withhold != 0 && tid == 0;  // test hook: one copy of the block never issued
-    uint8_t *dst = s_rows + (size_t)tl * tok_bytes;
-    for (int r = lane_t; r < R; r += tpt) {
-      const int ni = (r >= H) + (r >= 2 * H);
-      const int64_t id = ids[r];
-      if (withhold)
-        withhold = false;
-      else
-        bulk_g2s(dst + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
-      if (kE8) {
-        const uint8_t *e = static_cast<const uint8_t *>(p.scale[ni]) + id * exp_bytes;
-        uint8_t *se = s_exps + ((size_t)tl * R + r) * exp_bytes;
-        for (uint32_t c = 0; c < exp_bytes; ++c) se[c] = __ldg(e + c);
-      } else if (kFp8) {
-        s_scale[(size_t)tl * R + r] = __ldg(static_cast<const float *>(p.scale[ni]) + id);
-      }
-    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (lane_t + k * tpt < R) v[k] = issue_row(lane_t + k * tpt);
+    for (int r = lane_t + 4 * tpt; r < R; r += tpt) store_row(r, issue_row(r));
   }
   // The token's four stream slices, under the copies.
   uint4 xs[4][2];
@@ -440,6 +471,9 @@ __global__ void __launch_bounds__(256, 2)
       xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
       xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (lane_t + k * tpt < R) store_row(lane_t + k * tpt, v[k]);
   }
 
   const bool landed = wait_bounded(bar, p.wait_limit_ns);
@@ -582,11 +616,18 @@ size_t small_smem_bytes(int D, int dtype, int H, int tpb) {
   return rows * D * elt + ((exps + 15) & ~(size_t)15) + ((rows + 1) & ~(size_t)1) * 4 + 8;
 }
 
-// Tokens per block: up to 256 threads, within 56 KB of shared memory (four
-// blocks per SM: their copy, compute and store phases overlap better than two
-// larger blocks'), a whole number of warps.
+// Tokens per block, a whole number of warps.  Measured on the released shape
+// (256-wide FP8 rows with e8m0 blocks, 24 rows a token, 65,536 tokens): blocks
+// of three warps, five to an SM, took 157 us; every other size tried, from one
+// to seven warps a block and from two to sixteen blocks an SM (20 to 32 tokens
+// resident), took 166-197 us, the three-warp size with only four blocks an SM
+// among the slowest.  So: three warps when five such blocks fit in an SM's
+// 228 KB of shared memory (1 KB of each block's is reserved); else the largest
+// block of up to 256 threads within 56 KB (four blocks an SM).
 int small_tokens_per_block(int D, int dtype, int H) {
   const int tpt = D / 16, warp_tokens = 32 / tpt;
+  if (small_smem_bytes(D, dtype, H, 3 * warp_tokens) + 1024 <= 228 * 1024 / 5)
+    return 3 * warp_tokens;
   int tpb = 256 / tpt;
   while (tpb > warp_tokens && small_smem_bytes(D, dtype, H, tpb) > 56 * 1024) tpb -= warp_tokens;
   return tpb;
