@@ -1,11 +1,15 @@
 """Benchmark of the Engram hashed n-gram memory lookup on GB300.
 
 One step = the whole hot path over one batch: engram_compress -> engram_hash ->
-engram_lookup_fused, through the C ABI, on the full-size prefill workload
-(batch 8 x seq 8192 tokens, 8 hash heads, 4096-wide rows, three 5,040,000-row
-FP8 e4m3fn tables with fp32 row scales = 57.7 GiB, bf16 streams [8, 8192, 4, 4096]).
-Inputs are resident in HBM when the timed region starts; every input is larger
-than the 129 MB L2 (no flush needed).  The K timed steps are captured once into
+engram_lookup_fused, through the C ABI.  The default workload is the mid-size
+prefill (batch 4 x seq 4096 tokens, Zipf token ids, 4 hash heads, 4096-wide
+rows, three 1,000,000-row FP8 e4m3fn tables with fp32 row scales = 12.3 GB, bf16
+streams [4, 4096, 4, 4096]); --workload picks another (workloads.py: the
+full-size prefill of 65,536 tokens over 57.7 GiB of tables, a 512-slot decode
+step, BF16 tables, packed batches, e8m0 block scales, the released bucket
+layout, the wkv connection).  Inputs are resident in HBM when the timed region
+starts, larger than the 129 MB L2, or rotated among buffers when a step's
+streams fit in it.  The K timed steps are captured once into
 a CUDA graph and replayed (--eager launches them one by one from Python); CUDA
 events recorded inside the graph time the dominant kernel.  Prints ONE JSON
 line (rank 0).
@@ -35,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "full_prefill_fp8"
+DEFAULT_WORKLOAD = "mid_prefill_fp8"
 METRIC = "Engram fused lookup tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lookup_fused_traffic.json")
