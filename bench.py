@@ -387,21 +387,28 @@ def run_native(args):
     xs_rot = [d["streams"]] + [d["streams"].clone() for _ in range(n_rot - 1)]
     ys_rot = [step.out] + [torch.empty_like(step.out) for _ in range(n_rot - 1)]
     # The K timed steps are captured once into a CUDA graph and replayed, so the
-    # GPU runs them back to back without waiting on Python between launches;
-    # the events around each dominant-kernel launch are graph nodes that record
-    # (external events).
+    # GPU runs them back to back without waiting on Python between launches.
+    # The step throughput comes from a graph of the K steps alone; the dominant
+    # kernel's durations from a second replay of the same K steps, captured with
+    # CUDA events around each of its launches (external event nodes, which add
+    # their own few microseconds to a step and so stay out of the first graph).
     graphed = not args.eager and graph_timing_supported()
     ev_kw = {"enable_timing": True, "external": True} if graphed else {"enable_timing": True}
     ev = [(torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)) for _ in range(K)]
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    graph = None
+    graph = graph_ev = None
     if graphed:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(K):
+                step(x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            for i in range(K):
                 step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
         with torch.cuda.stream(stream):
-            graph.replay()   # untimed: the graph's first launch uploads it
+            graph.replay()       # untimed: a graph's first launch uploads it
+            graph_ev.replay()
         torch.cuda.synchronize()
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
@@ -418,6 +425,10 @@ def run_native(args):
             step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
     t_end.record(stream)
     torch.cuda.synchronize()
+    if graphed:   # the dominant kernel's durations: the same K steps with events
+        with torch.cuda.stream(stream):
+            graph_ev.replay()
+        torch.cuda.synchronize()
     wall1 = time.time()
     if world > 1:
         dist.barrier()
@@ -448,7 +459,20 @@ def run_native(args):
             # entry and the slot's history in and out instead
             bytes_tok += 4 + 4 + 12 + 12 - cfg.R * 4
         lk = statistics.mean(lookup_ms)
-        achieved = bytes_tok * cfg.T / (lk * 1e-3) / 1e9
+        # The dominant kernel's mean duration.  When a step is that one launch
+        # (the fused decode step), the timed region's own events hold exactly K
+        # back-to-back launches of it: their mean (gaps between launches
+        # included) is its duration, without the few microseconds an event node
+        # around each launch adds.  Otherwise, the events around its launches.
+        if step.launches == 1:
+            kernel_ms = ms_total / K
+            duration_source = ("timed region's CUDA events / K (each step is this one launch; "
+                               "gaps between the K launches included)")
+        else:
+            kernel_ms = lk
+            duration_source = ("CUDA events around each launch (event nodes in a second graph "
+                               "replay of the K steps; they add a few microseconds a launch)")
+        achieved = bytes_tok * cfg.T / (kernel_ms * 1e-3) / 1e9
         traffic = recorded_traffic(cfg, args.lookup_kernel)
         value = whole_job_throughput(world * cfg.T * K, ms_total * 1e-3)
         if cfg.hidden:
@@ -501,12 +525,16 @@ def run_native(args):
                 "traffic": traffic,
                 "algorithmic_bytes_per_token": bytes_tok,
                 "dead_tokens_per_step": n_dead,
+                "kernel_ms": kernel_ms,
+                "duration_source": duration_source,
                 "lookup_ms_mean": lk,
                 "lookup_ms_median": statistics.median(lookup_ms),
             },
             "gpu_launches": step.launches * K,
             "launch_mode": ("one CUDA graph of the K steps, replayed once (captured and "
-                            "replayed once untimed before)") if graphed else "eager",
+                            "replayed once untimed before); the dominant kernel timed in a "
+                            "second replay of the same K steps with CUDA events around its "
+                            "launches") if graphed else "eager (events around the dominant kernel)",
             "status_flags": flags,
             "clocks": clk,
         }

@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   __shared__ int s_skip, s_dead;
   const int64_t b = blockIdx.x;
   const int H = p.lk.H, R = 3 * H;
+  // The slot's streams do not depend on its token: their HBM reads start now,
+  // under the dependent loads of the token and its map entry.
+  if (threadIdx.x == 32) prefetch_l2(p.lk.x + b * 4 * p.lk.D, (uint32_t)(8 * p.lk.D));
   if (threadIdx.x == 0) {
     int32_t raw[3] = {0, 0, 0};
     if (p.history)
