@@ -174,11 +174,17 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
           static_cast<const uint8_t *>(p.scale[ni]) + (int64_t)ids[r] * exp_bytes) + c);
       *reinterpret_cast<uint4 *>(s_exps + (size_t)r * exp_bytes + 16 * c) = v;
     }
-  } else if (kFp8) {
-    for (int r = tid; r < R; r += blockDim.x) {
-      const int ni = (r >= H) + (r >= 2 * H);
-      s_scale[r] = __ldg(static_cast<const float *>(p.scale[ni]) + ids[r]);
-    }
+  }
+  // fp32 row scales: thread r loads row r's scale; with the streams loaded
+  // early it stores the scale only after issuing them (a store waits for its
+  // load, and the stream loads should not wait behind it: 0.952 -> 0.961 on
+  // the 8-head prefill; the same order for the e8m0 exponents measured 0.921 ->
+  // 0.914, so they keep theirs).
+  float sc = 0.f;
+  if (kFp8 && !kE8 && tid < R) {
+    const int ni = (tid >= H) + (tid >= 2 * H);
+    sc = __ldg(static_cast<const float *>(p.scale[ni]) + ids[tid]);
+    if (!EARLY) s_scale[tid] = sc;
   }
   uint4 xs[4][2];
   const uint16_t *xrow = p.x + t * 4 * D + col0;
@@ -187,6 +193,13 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
     for (int s = 0; s < 4; ++s) {
       xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
       xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
+    }
+  }
+  if (kFp8 && !kE8) {
+    if (EARLY && tid < R) s_scale[tid] = sc;
+    for (int r = tid + blockDim.x; r < R; r += blockDim.x) {
+      const int ni = (r >= H) + (r >= 2 * H);
+      s_scale[r] = __ldg(static_cast<const float *>(p.scale[ni]) + ids[r]);
     }
   }
 
