@@ -93,7 +93,7 @@ engram_status layout_buckets(const char *fn, const engram_tables *t, const engra
 
 // Compression (with the dead mask) and the hash (packed positions, prime
 // buckets) of a whole batch into eids and row ids, on `stream`.
-engram_status ids_to_rows(const char *fn, const int32_t *token_ids, int32_t batch, int32_t seq,
+engram_status ids_to_rows(const int32_t *token_ids, int32_t batch, int32_t seq,
                           const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
                           const int32_t *history, int32_t *history_out, int32_t n_heads,
                           const engram_tables *tables_host, const int32_t *positions,
@@ -106,7 +106,6 @@ engram_status ids_to_rows(const char *fn, const int32_t *token_ids, int32_t batc
   if (primes)
     return engram_hash_bucketed(eids, batch, seq, positions, history, history_out, n_heads, primes,
                                 rows, status, stream);
-  (void)fn;
   return engram_hash_packed(eids, batch, seq, positions, history, history_out, n_heads,
                             tables_host->rows, rows, status, stream);
 }
@@ -262,7 +261,7 @@ engram_status host_ids_to_rows(const char *fn, const HostIds &h, const int32_t *
     e = cudaMemcpyAsync(h.dead, dead_host, T, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess)
     return engram::set_error(ENGRAM_ERR_CUDA, "%s: ids copy: %s", fn, cudaGetErrorString(e));
-  return ids_to_rows(fn, h.ids, batch, seq, tid2eid, vocab, n_eids, history, history_out, n_heads,
+  return ids_to_rows(h.ids, batch, seq, tid2eid, vocab, n_eids, history, history_out, n_heads,
                      tables_host, pos_host ? h.positions : nullptr, dead_host ? h.dead : nullptr,
                      layout ? layout->primes : nullptr, h.eids, h.rows, status, s);
 }
@@ -324,7 +323,7 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
   }
   int32_t *eids = static_cast<int32_t *>(workspace);
   int32_t *rows = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + round_up(T * 4));
-  st = ids_to_rows("engram_forward", token_ids, batch, seq, tid2eid, vocab, n_eids, history,
+  st = ids_to_rows(token_ids, batch, seq, tid2eid, vocab, n_eids, history,
                    history_out, n_heads, tables_host,
                    layout_host ? layout_host->positions : nullptr,
                    layout_host ? layout_host->dead : nullptr,

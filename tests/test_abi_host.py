@@ -299,3 +299,28 @@ def test_library_bucket_primes_match_oracle_and_pages(eg):
     assert sum(sum(o) for o in eg.engram_bucket_primes(1, 4, 2, 64)[0]) == 462
     for args in [(2, 4, 8, 16_000_000), (1, 4, 3, 1000), (3, 5, 2, 97)]:
         assert (oracle.bucket_primes(*args).tolist() == eg.engram_bucket_primes(*args))
+
+
+def test_ctypes_structs_match_the_header(eg, tmp_path):
+    """The binding's engram_tables and engram_layout have the C structs' size and
+    field offsets, as gcc lays them out from include/engram.h."""
+    import ctypes
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "engram.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(engram_tables),\n'
+        "         offsetof(engram_tables, D), offsetof(engram_tables, rows),\n"
+        "         offsetof(engram_tables, table), offsetof(engram_tables, scale), 0ul);\n"
+        '  printf("%zu %zu %zu %zu\\n", sizeof(engram_layout), offsetof(engram_layout, positions),\n'
+        "         offsetof(engram_layout, dead), offsetof(engram_layout, primes));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    t = [int(v) for v in out[0].split()]
+    lay = [int(v) for v in out[1].split()]
+    T, L = eg.engram_tables, eg.engram_layout
+    assert t[:5] == [ctypes.sizeof(T), T.D.offset, T.rows.offset, T.table.offset, T.scale.offset]
+    assert lay == [ctypes.sizeof(L), L.positions.offset, L.dead.offset, L.primes.offset]
