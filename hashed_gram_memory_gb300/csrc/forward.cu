@@ -244,14 +244,9 @@ HostIds carve_host_ids(void *workspace, int64_t T, int32_t n_heads) {
   return h;
 }
 
-// Copies the host ids (and the layout's host positions and dead mask) in on
-// `s`, then compresses and hashes the whole batch there.
-engram_status host_ids_to_rows(const char *fn, const HostIds &h, const int32_t *token_ids_host,
-                               int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
-                               int32_t n_eids, const int32_t *history, int32_t *history_out,
-                               int32_t n_heads, const engram_tables *tables_host,
-                               const engram_layout *layout, int32_t *status, cudaStream_t s) {
-  const int64_t T = (int64_t)batch * seq;
+// Copies the host ids (and the layout's host positions and dead mask) in on `s`.
+engram_status copy_host_ids(const char *fn, const HostIds &h, const int32_t *token_ids_host,
+                            int64_t T, const engram_layout *layout, cudaStream_t s) {
   const int32_t *pos_host = layout ? layout->positions : nullptr;
   const uint8_t *dead_host = layout ? layout->dead : nullptr;
   cudaError_t e = cudaMemcpyAsync(h.ids, token_ids_host, T * 4, cudaMemcpyHostToDevice, s);
@@ -261,6 +256,21 @@ engram_status host_ids_to_rows(const char *fn, const HostIds &h, const int32_t *
     e = cudaMemcpyAsync(h.dead, dead_host, T, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess)
     return engram::set_error(ENGRAM_ERR_CUDA, "%s: ids copy: %s", fn, cudaGetErrorString(e));
+  return ENGRAM_OK;
+}
+
+// Copies the host ids (and layout) in on `s`, then compresses and hashes the
+// whole batch there.
+engram_status host_ids_to_rows(const char *fn, const HostIds &h, const int32_t *token_ids_host,
+                               int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
+                               int32_t n_eids, const int32_t *history, int32_t *history_out,
+                               int32_t n_heads, const engram_tables *tables_host,
+                               const engram_layout *layout, int32_t *status, cudaStream_t s) {
+  const int64_t T = (int64_t)batch * seq;
+  const int32_t *pos_host = layout ? layout->positions : nullptr;
+  const uint8_t *dead_host = layout ? layout->dead : nullptr;
+  const engram_status st = copy_host_ids(fn, h, token_ids_host, T, layout, s);
+  if (st != ENGRAM_OK) return st;
   return ids_to_rows(h.ids, batch, seq, tid2eid, vocab, n_eids, history, history_out, n_heads,
                      tables_host, pos_host ? h.positions : nullptr, dead_host ? h.dead : nullptr,
                      layout ? layout->primes : nullptr, h.eids, h.rows, status, s);
@@ -380,12 +390,37 @@ ENGRAM_API engram_status engram_forward_host(
   if (!hp) return ENGRAM_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const HostIds h = carve_host_ids(workspace, T, n_heads);
-  st = host_ids_to_rows(fn, h, token_ids_host, batch, seq, tid2eid, vocab, n_eids, history,
-                        history_out, n_heads, tables_host, layout_host, status, s);
-  if (st != ENGRAM_OK) return st;
   const int64_t chunk = chunk_tokens ? chunk_tokens : kDefaultChunk;
   const size_t tok_bytes = (size_t)4 * D * 2;
   const size_t buf = round_up(chunk * tok_bytes);
+  const int which = engram::lookup_kernel_choice();
+  if (seq == 1 && (which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
+      engram::bulk_supported(D, tables_host->dtype, n_heads)) {
+    // A decode step: each chunk of slots is one fused launch (compression,
+    // window, hash and lookup), as engram_forward runs it; only the ids move
+    // in ahead of the streams.
+    st = copy_host_ids(fn, h, token_ids_host, T, layout_host, s);
+    if (st != ENGRAM_OK) return st;
+    const int32_t *pos = layout_host && layout_host->positions ? h.positions : nullptr;
+    const uint8_t *dead = layout_host && layout_host->dead ? h.dead : nullptr;
+    const int64_t *primes = layout_host ? layout_host->primes : nullptr;
+    return run_chunks(fn, *hp, s, T, chunk, tok_bytes, h.rest, h.rest + kBufs * buf, buf,
+                      streams_in_host, streams_out_host,
+                      [&](int64_t t0, int64_t n, char *ib, char *ob) {
+                        const engram_layout lay = {pos ? pos + t0 : nullptr,
+                                                   dead ? dead + t0 : nullptr, primes};
+                        return decode_step(h.ids + t0, (int32_t)n, tid2eid, vocab, n_eids,
+                                           history ? history + t0 * 3 : nullptr,
+                                           history_out ? history_out + t0 * 3 : nullptr, n_heads,
+                                           tables_host, &lay,
+                                           reinterpret_cast<const uint16_t *>(ib),
+                                           reinterpret_cast<uint16_t *>(ob), alpha, eps, status,
+                                           stream);
+                      });
+  }
+  st = host_ids_to_rows(fn, h, token_ids_host, batch, seq, tid2eid, vocab, n_eids, history,
+                        history_out, n_heads, tables_host, layout_host, status, s);
+  if (st != ENGRAM_OK) return st;
   const int R = 3 * n_heads;
   return run_chunks(fn, *hp, s, T, chunk, tok_bytes, h.rest, h.rest + kBufs * buf, buf,
                     streams_in_host, streams_out_host,

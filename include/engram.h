@@ -377,6 +377,8 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
  * internal copy stream, the fused lookup on `stream`, device->host copies on a
  * second copy stream, with three chunk buffers per direction in `workspace`
  * (device memory of at least engram_forward_host_workspace_bytes(...) bytes).
+ * A decode step (seq == 1) that engram_forward would run as one fused launch
+ * runs each chunk of slots as that launch instead of compress + hash + lookup.
  * Returns once everything is enqueued; `stream` is ordered after the last
  * device->host copy, so synchronising `stream` means streams_out_host is final.
  * The two copy streams and their events are created on first use per device

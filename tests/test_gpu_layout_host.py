@@ -7,7 +7,8 @@ mask; the released prime-bucket table) and the host-buffer connection.
   too (positions cap the lookback, dead slots pass through, bucket moduli and
   offsets) and equals the three calls.
 * engram_forward_host with host positions and dead mask equals engram_forward
-  with the same layout on device buffers, for ragged chunk sizes.
+  with the same layout on device buffers, for ragged chunk sizes, and for
+  decode steps (each chunk of slots one fused launch), history included.
 * engram_connection_host (host ids and streams, chunked copies overlapped with
   the connection) equals compress -> hash -> engram_connection on device
   buffers bit for bit: plain and bucketed tables, packed batches with dead
@@ -212,3 +213,45 @@ def test_connection_host_equals_device_connection(eg, name, chunk, pinned):
     assert eg.engram_read_status(st)[1] == 0
     for ids_h, x_h, y_h, pos_h, dead_h, dev, wkv, ref in calls:
         assert np.array_equal(y_h.numpy().view(np.uint16).reshape(ref.shape), ref)
+
+
+@pytest.mark.parametrize("primes,chunk", [(False, 0), (True, 100)])
+def test_forward_host_decode_with_layout_equals_forward(eg, primes, chunk):
+    """A decode step through engram_forward_host (each chunk of slots one fused
+    launch) with host positions and dead mask, and optionally the bucket layout,
+    equals engram_forward on device buffers: streams and history bit for bit."""
+    import torch
+    B = 301
+    base = W.by_name("decode_fp8").scaled(B=B, H=4, rows=(32_000,) * 3)
+    cfg = base.scaled(hash_vocab=1000) if primes else base
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    g = np.random.default_rng(78)
+    pos = g.integers(0, 6, size=(B, 1)).astype(np.int32)
+    dead = (g.random((B, 1)) < 0.125).astype(np.uint8)
+    pr = _primes(eg, cfg)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h_dev = torch.empty_like(dev["history"])
+    y_dev = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                              dev["streams"], dev["alpha"], cfg.eps, history=dev["history"],
+                              history_out=h_dev, status=st, positions=torch.from_numpy(pos).cuda(),
+                              dead=torch.from_numpy(dead).cuda(), primes=pr)
+    ids_h = torch.from_numpy(inp.ids).pin_memory()
+    x_h = torch.from_numpy(inp.streams.view(np.int16)).reshape(cfg.T, 4, cfg.D).pin_memory()
+    y_h = torch.full_like(x_h, 0x7777).pin_memory()
+    h_host = torch.empty_like(dev["history"])
+    ws = torch.empty(eg.engram_forward_host_workspace_bytes(cfg.B, cfg.S, cfg.H, cfg.D, chunk),
+                     dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        eg.engram_forward_host(ids_h, dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"], x_h, y_h,
+                               dev["alpha"], ws, cfg.eps, history=dev["history"],
+                               history_out=h_host, chunk_tokens=chunk, status=st,
+                               positions=torch.from_numpy(pos).pin_memory(),
+                               dead=torch.from_numpy(dead).pin_memory(), primes=pr)
+    stream.synchronize()
+    assert eg.engram_read_status(st)[1] == 0
+    assert np.array_equal(y_h.numpy().view(np.uint16).reshape(cfg.T, -1),
+                          y_dev.cpu().numpy().view(np.uint16).reshape(cfg.T, -1))
+    assert torch.equal(h_host, h_dev)
