@@ -1,7 +1,7 @@
 """Benchmark of the Engram hashed n-gram memory lookup on GB300.
 
-One step = the whole hot path over one batch: engram_compress -> engram_hash ->
-engram_lookup_fused, through the C ABI.  The default workload is the mid-size
+One step = the whole hot path over one batch through the C ABI:
+engram_compress_hash (compression and hash in one launch) -> engram_lookup_fused.  The default workload is the mid-size
 prefill (batch 4 x seq 4096 tokens, Zipf token ids, 4 hash heads, 4096-wide
 rows, three 1,000,000-row FP8 e4m3fn tables with fp32 row scales = 12.3 GB, bf16
 streams [4, 4096, 4, 4096]); --workload picks another (workloads.py: the
@@ -262,20 +262,22 @@ def device_inputs(eg, cfg, rank, device):
 
 
 class Step:
-    """Pre-allocated buffers and the three C-ABI calls of one step."""
+    """Pre-allocated buffers and the C-ABI calls of one step: the compression and
+    hash in one launch (engram_compress_hash), then the fused lookup (or the
+    connection's three stages); a decode step is the one fused launch of
+    engram_forward."""
 
     def __init__(self, eg, cfg, d, stream):
         import torch
         self.eg, self.cfg, self.d, self.stream = eg, cfg, d, stream
         dev = d["streams"].device
-        self.eids = torch.empty_like(d["ids"])
         self.rows = torch.empty((cfg.B, cfg.S, 3, cfg.H), dtype=torch.int32, device=dev)
         self.hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
         self.out = torch.empty_like(d["streams"])
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.primes = (eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0]
                        if cfg.hash_vocab else None)
-        self.launches = 3
+        self.launches = 2
         # One new token a slot: the one-call engram_forward, which runs the decode
         # step as one fused launch (compress, window, hash and lookup).
         self.fused_decode = (cfg.S == 1 and not cfg.hidden and cfg.D % 512 == 0 and
@@ -288,7 +290,7 @@ class Step:
             self.e = torch.empty((cfg.T, cfg.K), dtype=torch.bfloat16, device=dev)
             self.state = torch.empty((cfg.T,), dtype=torch.uint8, device=dev)
             self.k = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
-            self.launches = 5
+            self.launches = 4
 
     def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None):
         eg, cfg, d = self.eg, self.cfg, self.d
@@ -306,11 +308,10 @@ class Step:
             if ev_end is not None:
                 ev_end.record(self.stream)
             return
-        eg.engram_compress(ids, d["tid2eid"], cfg.n_eids, eids_out=self.eids, status=self.status,
-                           stream=self.stream, dead=d["dead"])
-        eg.engram_hash(self.eids, cfg.H, cfg.rows, history=d["history"], history_out=self.hist_out,
-                       row_ids_out=self.rows, status=self.status, stream=self.stream,
-                       positions=d["positions"], primes=self.primes)
+        eg.engram_compress_hash(ids, d["tid2eid"], cfg.n_eids, cfg.H, cfg.rows,
+                                history=d["history"], history_out=self.hist_out,
+                                row_ids_out=self.rows, status=self.status, stream=self.stream,
+                                positions=d["positions"], dead=d["dead"], primes=self.primes)
         if cfg.hidden:
             eg.engram_concat_rows(self.rows, cfg.H, d["tables"], e_out=self.e,
                                   state_out=self.state, status=self.status, stream=self.stream)

@@ -76,7 +76,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build the CUDA library first "
-            "(python -m hashed_gram_memory_gb300.build, or __graft_entry__.build())")
+            "(python hashed_gram_memory_gb300/build.py, or __graft_entry__.build())")
     L = C.CDLL(LIB_PATH)
     vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
     L.engram_compress.argtypes = [vp, i64, vp, i32, i32, vp, vp, vp]
@@ -87,12 +87,15 @@ def _load():
     L.engram_hash_bucketed.argtypes = [vp, i32, i32, vp, vp, vp, i32, C.POINTER(C.c_int64), vp, vp,
                                        vp]
     L.engram_bucket_primes.argtypes = [i32, i32, i32, i64, C.POINTER(C.c_int64)]
+    L.engram_compress_hash.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32,
+                                       C.POINTER(C.c_int64), C.POINTER(engram_layout), vp, vp, vp,
+                                       vp]
     L.engram_lookup_fused.argtypes = [vp, i64, i32, C.POINTER(engram_tables), vp, vp, vp,
                                       C.c_float, vp, vp, vp, vp]
     L.engram_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
     for f in ("engram_compress", "engram_compress_masked", "engram_hash", "engram_hash_packed",
-              "engram_hash_bucketed", "engram_bucket_primes", "engram_lookup_fused",
-              "engram_read_status"):
+              "engram_hash_bucketed", "engram_bucket_primes", "engram_compress_hash",
+              "engram_lookup_fused", "engram_read_status"):
         getattr(L, f).restype = C.c_int32
     L.engram_status_string.argtypes = [C.c_int32]
     L.engram_status_string.restype = C.c_char_p
@@ -262,6 +265,33 @@ def engram_hash(eids, n_heads: int, rows, history=None, history_out=None, row_id
     _check(lib.engram_hash_packed(_ptr(eids), B, S, _ptr(positions), _ptr(history),
                                   _ptr(history_out), n_heads, r, _ptr(row_ids_out), _ptr(status),
                                   _stream(stream)), "engram_hash")
+    return row_ids_out
+
+
+def engram_compress_hash(token_ids, tid2eid, n_eids: int, n_heads: int, rows, history=None,
+                         history_out=None, row_ids_out=None, eids_out=None, status=None,
+                         stream=None, positions=None, dead=None, primes=None):
+    """Compression and hash in one launch: row ids [B, S, 3, n_heads] int32 for token
+    ids [B, S]; positions / dead (device) and primes as for engram_forward;
+    eids_out (optional, int32 [B, S]) receives the compressed ids."""
+    import torch
+    _need(token_ids, (torch.int32,), "token_ids")
+    _need(tid2eid, (torch.int32,), "tid2eid")
+    if token_ids.dim() != 2:
+        raise EngramError(ERR_INVALID_ARG, "token_ids must be [batch, seq]")
+    B, S = token_ids.shape
+    if row_ids_out is None:
+        row_ids_out = torch.empty((B, S, 3, n_heads), dtype=torch.int32, device=token_ids.device)
+    _need(row_ids_out, (torch.int32,), "row_ids_out")
+    _need(eids_out, (torch.int32,), "eids_out")
+    _need(history, (torch.int32,), "history")
+    _need(history_out, (torch.int32,), "history_out")
+    r = (C.c_int64 * 3)(*[int(x) for x in rows])
+    lay = _layout(positions, dead, primes, host=False)
+    _check(lib.engram_compress_hash(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
+                                    _ptr(history), _ptr(history_out), n_heads, r, _ref(lay),
+                                    _ptr(eids_out), _ptr(row_ids_out), _ptr(status),
+                                    _stream(stream)), "engram_compress_hash")
     return row_ids_out
 
 

@@ -2,7 +2,8 @@
 
 Each .cu translation unit is compiled by nvcc in parallel, then linked into
 hashed_gram_memory_gb300/libengram.so with the CUDA runtime linked statically.
-Run: python -m hashed_gram_memory_gb300.build [--force] [--verbose]
+Run as a script (importing the package needs the library it builds):
+  python hashed_gram_memory_gb300/build.py [--force] [--verbose] [--ptxas]
 """
 from __future__ import annotations
 

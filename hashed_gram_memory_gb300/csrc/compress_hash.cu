@@ -42,6 +42,27 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   flag_warp(p.status, flags);
 }
 
+// The compressed id of position i when the hash compresses its own inputs: the
+// dead id for a dead position (no range check), else the map's value, or
+// kBadEid (below the dead id, so a window that reaches it is bad) with the
+// reason in *why.
+constexpr int32_t kBadEid = INT32_MIN;
+
+__device__ __forceinline__ int32_t compress_at(const HashParams &p, int64_t i, uint32_t &why) {
+  if (p.dead && p.dead[i]) return ENGRAM_EID_DEAD;
+  const int32_t tok = __ldg(p.token_ids + i);
+  if ((uint32_t)tok >= (uint32_t)p.vocab) {
+    why = ENGRAM_FLAG_BAD_TOKEN;
+    return kBadEid;
+  }
+  const int32_t e = __ldg(p.tid2eid + tok);
+  if (e < 0 || e > p.n_eids) {
+    why = ENGRAM_FLAG_BAD_EID;
+    return kBadEid;
+  }
+  return e;
+}
+
 // One thread per token.  The thread reads the token's window once, back from
 // the token until its lookback limit (its position in its sample if positions
 // are given, else 3 with a history and s without) or a dead id, whichever comes
@@ -52,8 +73,13 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
 // ENGRAM_ROW_DEAD.  The ids are staged in shared memory at an odd stride
 // (conflict-free) and stored by the whole block, so that the stores are
 // contiguous: the block's tokens own one contiguous range of row_ids.
+// COMPRESS: the window's token ids are compressed here (the map is L2-resident,
+// the neighbours' ids L1 hits), so no separate compression pass runs; a token
+// whose own id or map value is out of range flags its reason, and every token
+// whose window reaches it is left unwritten.
 constexpr int kHashTokens = 64;
 
+template <bool COMPRESS>
 __global__ void __launch_bounds__(kHashTokens) hash_kernel(const __grid_constant__ HashParams p) {
   extern __shared__ int32_t s_rows[];  // [kHashTokens][stride], then [kHashTokens] skip flags
   const int R = 3 * p.H, stride = R | 1;
@@ -67,17 +93,27 @@ __global__ void __launch_bounds__(kHashTokens) hash_kernel(const __grid_constant
     const int s = (int)(t - (int64_t)b * p.seq);
     const int64_t base = (int64_t)b * p.seq;
     int32_t raw[4] = {0, 0, 0, 0};  // the ids s-3 .. s as stored (for history_out)
+    uint32_t why = 0;               // COMPRESS: why the token's own id is bad
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int pos = s - 3 + k;
-      if (pos >= 0)
-        raw[k] = __ldg(p.eids + base + pos);
-      else if (p.history)
+      if (pos >= 0) {
+        if (COMPRESS) {
+          uint32_t w_k = 0;
+          raw[k] = compress_at(p, base + pos, w_k);
+          if (k == 3) why = w_k;
+        } else {
+          raw[k] = __ldg(p.eids + base + pos);
+        }
+      } else if (p.history) {
         raw[k] = p.history[(int64_t)b * 3 + 3 + pos];  // plain load: history may be rewritten below
+      }
     }
     const int32_t self = raw[3];
     const bool dead = self == ENGRAM_EID_DEAD;
+    const bool self_bad = COMPRESS && self == kBadEid;
     bool bad = self < ENGRAM_EID_DEAD;
+    if (COMPRESS && !self_bad && p.eids_out) p.eids_out[t] = self;
     int32_t w[4] = {0, 0, 0, 0};  // oldest first, w[3] = the token's own id
     if (!dead && !bad) {
       // positions before 0 hold the history or 0 (raw), so the limit alone decides
@@ -87,14 +123,14 @@ __global__ void __launch_bounds__(kHashTokens) hash_kernel(const __grid_constant
     }
     int32_t *mine = s_rows + threadIdx.x * stride;
     if (bad) {
-      flags = ENGRAM_FLAG_BAD_EID;
+      flags = self_bad ? why : ENGRAM_FLAG_BAD_EID;
     } else if (dead) {
       for (int r = 0; r < R; ++r) mine[r] = ENGRAM_ROW_DEAD;
     } else {
       for (int r = 0; r < R; ++r) mine[r] = window_row(w, r, p.H, p.seed, p.mod, p.rmul, p.off);
     }
     skip = bad;
-    if (p.history_inline) {
+    if (p.history_inline && !self_bad) {
       // seq == 1: this thread is the only reader of history[b], and it is done.
 #pragma unroll
       for (int k = 0; k < 3; ++k) p.history_out[(int64_t)b * 3 + k] = raw[k + 1];
@@ -121,19 +157,32 @@ __global__ void __launch_bounds__(kHashTokens) hash_kernel(const __grid_constant
 
 // history_out[b] = last three ids of history[b] ++ eids[b]; one thread per
 // sequence, all reads before any write (history_out may be history).
-__global__ void history_kernel(const int32_t *eids, const int32_t *history, int32_t *history_out,
-                               int32_t batch, int32_t seq) {
+// COMPRESS: the last three ids are compressed here; a sequence whose tail holds
+// a bad id keeps its history_out unwritten (the hash flagged it).
+template <bool COMPRESS>
+__global__ void history_kernel(const __grid_constant__ HashParams p) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= batch) return;
+  if (b >= p.batch) return;
   int32_t tail[3];
+  bool ok = true;
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
-    const int pos = seq - 3 + k;
-    tail[k] = pos >= 0 ? eids[(int64_t)b * seq + pos]
-                       : (history ? history[(int64_t)b * 3 + 3 + pos] : 0);
+    const int pos = p.seq - 3 + k;
+    if (pos >= 0) {
+      if (COMPRESS) {
+        uint32_t why = 0;
+        tail[k] = compress_at(p, (int64_t)b * p.seq + pos, why);
+        ok = ok && tail[k] != kBadEid;
+      } else {
+        tail[k] = p.eids[(int64_t)b * p.seq + pos];
+      }
+    } else {
+      tail[k] = p.history ? p.history[(int64_t)b * 3 + 3 + pos] : 0;
+    }
   }
+  if (!ok) return;
 #pragma unroll
-  for (int k = 0; k < 3; ++k) history_out[(int64_t)b * 3 + k] = tail[k];
+  for (int k = 0; k < 3; ++k) p.history_out[(int64_t)b * 3 + k] = tail[k];
 }
 
 }  // namespace
@@ -157,19 +206,25 @@ cudaError_t launch_compress(const CompressParams &p, cudaStream_t stream) {
 cudaError_t launch_hash(const HashParams &p_in, cudaStream_t stream) {
   HashParams p = p_in;
   const int R = 3 * p.H;
+  const bool compress = p.token_ids != nullptr;
   p.tokens_per_block = kHashTokens;
   p.history_inline = (p.history_out != nullptr && p.seq == 1) ? 1 : 0;
   if (p.T > 0) {
     // kHashTokens is whole warps: flag_warp reduces over full warps.
     const size_t smem = (size_t)kHashTokens * ((R | 1) + 1) * sizeof(int32_t);
     const int64_t blocks = (p.T + kHashTokens - 1) / kHashTokens;
-    hash_kernel<<<(unsigned)blocks, kHashTokens, smem, stream>>>(p);
+    if (compress)
+      hash_kernel<true><<<(unsigned)blocks, kHashTokens, smem, stream>>>(p);
+    else
+      hash_kernel<false><<<(unsigned)blocks, kHashTokens, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (p.history_out != nullptr && !p.history_inline && p.batch > 0) {
-    history_kernel<<<(p.batch + 127) / 128, 128, 0, stream>>>(p.eids, p.history, p.history_out,
-                                                               p.batch, p.seq);
+    if (compress)
+      history_kernel<true><<<(p.batch + 127) / 128, 128, 0, stream>>>(p);
+    else
+      history_kernel<false><<<(p.batch + 127) / 128, 128, 0, stream>>>(p);
     return cudaGetLastError();
   }
   return cudaSuccess;

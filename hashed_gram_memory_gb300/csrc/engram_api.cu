@@ -133,13 +133,24 @@ ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tok
                                 status, stream);
 }
 
+// The compression inputs of engram_compress_hash (the hash then reads token ids
+// and compresses them itself instead of reading eids).
+struct FusedCompress {
+  const int32_t *token_ids;
+  const int32_t *tid2eid;
+  const uint8_t *dead;
+  int32_t *eids_out;
+  int32_t vocab, n_eids;
+};
+
 // Shared validation and launch of the hash: mod/off are the per-(order, head)
-// modulus and offset of every row id (host arrays of 3 * n_heads).
+// modulus and offset of every row id (host arrays of 3 * n_heads).  With `fc`
+// the ids come from token ids compressed in the kernel, and `eids` is unused.
 static engram_status hash_common(const char *fn, const int32_t *eids, int32_t batch, int32_t seq,
                                  const int32_t *positions, const int32_t *history,
                                  int32_t *history_out, int32_t n_heads, const int64_t *mod,
                                  const int64_t *off, int32_t *row_ids_out, int32_t *status,
-                                 void *stream) {
+                                 void *stream, const FusedCompress *fc = nullptr) {
   if (batch < 0 || seq < 0) return fail(ENGRAM_ERR_INVALID_ARG, "%s: batch or seq < 0", fn);
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
@@ -148,7 +159,31 @@ static engram_status hash_common(const char *fn, const int32_t *eids, int32_t ba
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: row ids must fit [0, 2^31-1] (bucket %d)", fn, r);
   const int64_t T = (int64_t)batch * seq;
   const size_t R = 3 * (size_t)n_heads;
-  if (T > 0 && (!eids || !row_ids_out))
+  if (fc) {
+    // The compression's own checks; eids_out is an output beside the row ids.
+    if (fc->vocab < 1 || fc->n_eids < 0 || !fc->tid2eid)
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: vocab < 1, n_eids < 0 or tid2eid NULL", fn);
+    if (T > 0 && !fc->token_ids)
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: token_ids is NULL", fn);
+    if (!aligned(fc->token_ids, 4) || !aligned(fc->tid2eid, 4) || !aligned(fc->eids_out, 4))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: int32 pointers must be 4-byte aligned", fn);
+    const size_t tb = (size_t)T * 4;
+    if (fc->eids_out && (overlap(fc->eids_out, tb, fc->token_ids, tb) ||
+                         overlap(fc->eids_out, tb, fc->tid2eid, (size_t)fc->vocab * 4) ||
+                         overlap(fc->eids_out, tb, fc->dead, (size_t)T) ||
+                         overlap(fc->eids_out, tb, row_ids_out, T * R * 4) ||
+                         overlap(fc->eids_out, tb, history_out, (size_t)batch * 12) ||
+                         overlap(fc->eids_out, tb, history, (size_t)batch * 12) ||
+                         overlap(fc->eids_out, tb, positions, tb)))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: eids_out overlaps another buffer", fn);
+    if (overlap(row_ids_out, T * R * 4, fc->token_ids, tb) ||
+        overlap(row_ids_out, T * R * 4, fc->dead, (size_t)T) ||
+        (history_out && (overlap(history_out, (size_t)batch * 12, fc->token_ids, tb) ||
+                         overlap(history_out, (size_t)batch * 12, fc->dead, (size_t)T))))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: an output overlaps token_ids or the dead mask", fn);
+    eids = nullptr;
+  }
+  if (T > 0 && ((!eids && !fc) || !row_ids_out))
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: eids or row_ids_out is NULL", fn);
   if (!aligned(eids, 4) || !aligned(history, 4) || !aligned(history_out, 4) ||
       !aligned(row_ids_out, 4) || !aligned(status, 4))
@@ -182,6 +217,14 @@ static engram_status hash_common(const char *fn, const int32_t *eids, int32_t ba
   p.batch = batch;
   p.seq = seq;
   p.H = n_heads;
+  if (fc) {
+    p.token_ids = fc->token_ids;
+    p.tid2eid = fc->tid2eid;
+    p.dead = fc->dead;
+    p.eids_out = fc->eids_out;
+    p.vocab = fc->vocab;
+    p.n_eids = fc->n_eids;
+  }
   for (int n = 0; n < 3; ++n)
     for (int j = 0; j < n_heads; ++j) {
       const int r = n * n_heads + j;
@@ -237,6 +280,40 @@ ENGRAM_API engram_status engram_hash_bucketed(const int32_t *eids, int32_t batch
                 (long long)sum);
   return hash_common("engram_hash_bucketed", eids, batch, seq, positions, history, history_out,
                      n_heads, primes_host, off, row_ids_out, status, stream);
+}
+
+ENGRAM_API engram_status engram_compress_hash(
+    const int32_t *token_ids, int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
+    int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
+    const int64_t *rows_host, const engram_layout *layout_host, int32_t *eids_out,
+    int32_t *row_ids_out, int32_t *status, void *stream) {
+  const char *fn = "engram_compress_hash";
+  if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
+  const int64_t *primes = layout_host ? layout_host->primes : nullptr;
+  int64_t mod[3 * ENGRAM_MAX_HEADS], off[3 * ENGRAM_MAX_HEADS];
+  int64_t sum = 0;
+  for (int n = 0; n < 3; ++n) {
+    if (!primes && (!rows_host || rows_host[n] < 1 || rows_host[n] > INT32_MAX))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: rows must be in [1, 2^31-1]", fn);
+    for (int j = 0; j < n_heads; ++j) {
+      const int r = n * n_heads + j;
+      if (primes) {
+        if (primes[r] < 1 || primes[r] > INT32_MAX)
+          return fail(ENGRAM_ERR_INVALID_ARG, "%s: bucket %d size out of range", fn, r);
+        mod[r] = primes[r];
+        off[r] = sum;
+        sum += primes[r];
+      } else {
+        mod[r] = rows_host[n];
+        off[r] = 0;
+      }
+    }
+  }
+  const FusedCompress fc{token_ids, tid2eid, layout_host ? layout_host->dead : nullptr, eids_out,
+                         vocab, n_eids};
+  return hash_common(fn, nullptr, batch, seq, layout_host ? layout_host->positions : nullptr,
+                     history, history_out, n_heads, mod, off, row_ids_out, status, stream, &fc);
 }
 
 // Trial division: no divisor d with d*d <= n.

@@ -35,6 +35,14 @@ struct HashParams {
   int32_t batch, seq, H;
   int32_t tokens_per_block;  // tokens whose 3H outputs one block owns
   int32_t history_inline;    // 1: seq == 1 and the block writes history_out itself
+  // Compression fused in (token_ids non-NULL): the ids of each window are
+  // compressed where they are read (eids is then not read), and eids_out
+  // (optional) receives each token's compressed id.
+  const int32_t *token_ids;
+  const int32_t *tid2eid;
+  const uint8_t *dead;
+  int32_t *eids_out;
+  int32_t vocab, n_eids;
   // Row r = (n-2)*H + j of a token is off[n-2][j] + (h mod mod[n-2][j]):
   // one table per order (off 0, mod rows_n) or one table cut into prime buckets.
   uint64_t mod[3][kMaxHeads];

@@ -92,22 +92,16 @@ engram_status layout_buckets(const char *fn, const engram_tables *t, const engra
 }
 
 // Compression (with the dead mask) and the hash (packed positions, prime
-// buckets) of a whole batch into eids and row ids, on `stream`.
+// buckets) of a whole batch into row ids, on `stream`, as one launch.
 engram_status ids_to_rows(const int32_t *token_ids, int32_t batch, int32_t seq,
                           const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
                           const int32_t *history, int32_t *history_out, int32_t n_heads,
                           const engram_tables *tables_host, const int32_t *positions,
-                          const uint8_t *dead, const int64_t *primes, int32_t *eids,
-                          int32_t *rows, int32_t *status, void *stream) {
-  const int64_t T = (int64_t)batch * seq;
-  engram_status st = engram_compress_masked(token_ids, T, tid2eid, vocab, n_eids, dead, eids,
-                                            status, stream);
-  if (st != ENGRAM_OK) return st;
-  if (primes)
-    return engram_hash_bucketed(eids, batch, seq, positions, history, history_out, n_heads, primes,
-                                rows, status, stream);
-  return engram_hash_packed(eids, batch, seq, positions, history, history_out, n_heads,
-                            tables_host->rows, rows, status, stream);
+                          const uint8_t *dead, const int64_t *primes, int32_t *rows,
+                          int32_t *status, void *stream) {
+  const engram_layout lay = {positions, dead, primes};
+  return engram_compress_hash(token_ids, batch, seq, tid2eid, vocab, n_eids, history, history_out,
+                              n_heads, tables_host->rows, &lay, nullptr, rows, status, stream);
 }
 
 // One decode step (one new token a slot) in one launch: compression, window,
@@ -273,7 +267,7 @@ engram_status host_ids_to_rows(const char *fn, const HostIds &h, const int32_t *
   if (st != ENGRAM_OK) return st;
   return ids_to_rows(h.ids, batch, seq, tid2eid, vocab, n_eids, history, history_out, n_heads,
                      tables_host, pos_host ? h.positions : nullptr, dead_host ? h.dead : nullptr,
-                     layout ? layout->primes : nullptr, h.eids, h.rows, status, s);
+                     layout ? layout->primes : nullptr, h.rows, status, s);
 }
 
 // The per-device pipe, locked for the call; NULL (error set) if it cannot be made.
@@ -331,13 +325,12 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
                          tables_host, layout_host, streams_in, streams_out, alpha, eps, status,
                          stream);
   }
-  int32_t *eids = static_cast<int32_t *>(workspace);
   int32_t *rows = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + round_up(T * 4));
   st = ids_to_rows(token_ids, batch, seq, tid2eid, vocab, n_eids, history,
                    history_out, n_heads, tables_host,
                    layout_host ? layout_host->positions : nullptr,
                    layout_host ? layout_host->dead : nullptr,
-                   layout_host ? layout_host->primes : nullptr, eids, rows, status, stream);
+                   layout_host ? layout_host->primes : nullptr, rows, status, stream);
   if (st != ENGRAM_OK) return st;
   return engram_lookup_fused(rows, T, n_heads, tables_host, streams_in, streams_out, alpha, eps,
                              nullptr, nullptr, status, stream);

@@ -163,7 +163,7 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
     if (!EARLY && lane == 0) prefetch_l2(p.x + t * 4 * D, (uint32_t)(8 * D));
   }
   // Meanwhile: the row scales into shared memory, the stream slices into registers.
-  if (kE8) {
+  if constexpr (kE8) {
     // The rows' block exponents (D/32 bytes each, a multiple of 16 here), 16
     // bytes per thread, coalesced: their latency overlaps the row copies.
     const int per_row = (int)exp_bytes / 16;

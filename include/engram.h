@@ -217,6 +217,32 @@ ENGRAM_API engram_status engram_hash_bucketed(const int32_t *eids, int32_t batch
                                               int32_t *status, void *stream);
 
 /*
+ * engram_compress_hash -- engram_compress_masked then engram_hash_packed (or
+ * engram_hash_bucketed) as one launch: the hash compresses the ids of every
+ * window itself (the map is small and stays cached), so the compressed ids make
+ * no round trip through memory.  For valid input the row ids, history_out and
+ * (when eids_out is given) the compressed ids equal those of the two calls.
+ *   token_ids   int32 [batch, seq] (device); tid2eid, vocab, n_eids as for
+ *               engram_compress
+ *   history, history_out, n_heads, row_ids_out as for engram_hash
+ *   rows_host   as for engram_hash; not read when layout_host->primes is given
+ *   layout_host positions and dead mask in DEVICE memory, bucket primes on the
+ *               host (engram_layout, below); NULL for the plain case
+ *   eids_out    int32 [batch, seq] or NULL: the compressed ids
+ * A token id outside [0, vocab) sets ENGRAM_FLAG_BAD_TOKEN, a map value outside
+ * [0, n_eids] ENGRAM_FLAG_BAD_EID; that token's compressed id and row ids stay
+ * unwritten, as do the row ids of every token whose window reaches it
+ * (ENGRAM_FLAG_BAD_EID) and history_out of a sequence whose last three ids
+ * hold it.  None of the outputs may overlap an input.
+ */
+struct engram_layout;
+ENGRAM_API engram_status engram_compress_hash(
+    const int32_t *token_ids, int32_t batch, int32_t seq, const int32_t *tid2eid, int32_t vocab,
+    int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
+    const int64_t *rows_host, const struct engram_layout *layout_host, int32_t *eids_out,
+    int32_t *row_ids_out, int32_t *status, void *stream);
+
+/*
  * engram_lookup_fused -- gather + dequantise the 3*n_heads rows of every token,
  * average them into m, gate with g = sigmoid(<rmsnorm(stream0), rmsnorm(m)> /
  * sqrt(D)) and add g * alpha_s * m into the four mHC streams (VeOmni PR page:

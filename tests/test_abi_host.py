@@ -324,3 +324,37 @@ def test_ctypes_structs_match_the_header(eg, tmp_path):
     T, L = eg.engram_tables, eg.engram_layout
     assert t[:5] == [ctypes.sizeof(T), T.D.offset, T.rows.offset, T.table.offset, T.scale.offset]
     assert lay == [ctypes.sizeof(L), L.positions.offset, L.dead.offset, L.primes.offset]
+
+
+def test_compress_hash_argument_errors(eg):
+    """engram_compress_hash checks the compression's and the hash's arguments on
+    the host, before any device query."""
+    L = eg.lib
+    INV, OK = eg.ERR_INVALID_ARG, eg.OK
+    tok, m, rows_out, e_out = (C.c_void_p(v) for v in (0x10000, 0x80000, 0x200000, 0x400000))
+    rows = (C.c_int64 * 3)(11, 13, 17)
+
+    def ch(tok=tok, batch=2, seq=8, m=m, vocab=100, n_eids=50, H=2, rows=rows, lay=None,
+           e=None, out=rows_out, hist=None, hout=None):
+        return L.engram_compress_hash(tok, batch, seq, m, vocab, n_eids, hist, hout, H, rows,
+                                      C.byref(lay) if lay is not None else None, e, out, None,
+                                      None)
+
+    assert ch(tok=None) == INV
+    assert ch(m=None) == INV
+    assert ch(vocab=0) == INV
+    assert ch(n_eids=-1) == INV
+    assert ch(H=0) == INV
+    assert ch(rows=(C.c_int64 * 3)(11, 0, 17)) == INV
+    assert ch(tok=C.c_void_p(0x10002)) == INV              # misaligned
+    assert ch(e=C.c_void_p(0x10008)) == INV                # eids_out over the token ids
+    assert ch(e=C.c_void_p(0x200010)) == INV               # eids_out over the row ids
+    assert ch(out=C.c_void_p(0x10000)) == INV              # row ids over the token ids
+    assert ch(out=None) == INV
+    bad = eg.engram_layout()
+    bad._keep = (C.c_int64 * 6)(7, 11, 0, 13, 17, 19)
+    bad.primes = C.cast(bad._keep, C.POINTER(C.c_int64))
+    assert ch(lay=bad) == INV                             # a bucket of no rows
+    assert ch(batch=0) == OK                              # nothing to do
+    assert ch(seq=0, tok=None, out=None) == OK
+
