@@ -176,11 +176,15 @@ static engram_status hash_common(const char *fn, const int32_t *eids, int32_t ba
                          overlap(fc->eids_out, tb, history, (size_t)batch * 12) ||
                          overlap(fc->eids_out, tb, positions, tb)))
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: eids_out overlaps another buffer", fn);
+    const size_t mb = (size_t)fc->vocab * 4;
     if (overlap(row_ids_out, T * R * 4, fc->token_ids, tb) ||
         overlap(row_ids_out, T * R * 4, fc->dead, (size_t)T) ||
+        overlap(row_ids_out, T * R * 4, fc->tid2eid, mb) ||
         (history_out && (overlap(history_out, (size_t)batch * 12, fc->token_ids, tb) ||
-                         overlap(history_out, (size_t)batch * 12, fc->dead, (size_t)T))))
-      return fail(ENGRAM_ERR_INVALID_ARG, "%s: an output overlaps token_ids or the dead mask", fn);
+                         overlap(history_out, (size_t)batch * 12, fc->dead, (size_t)T) ||
+                         overlap(history_out, (size_t)batch * 12, fc->tid2eid, mb))))
+      return fail(ENGRAM_ERR_INVALID_ARG, "%s: an output overlaps token_ids, tid2eid or the dead mask",
+                  fn);
     eids = nullptr;
   }
   if (T > 0 && ((!eids && !fc) || !row_ids_out))

@@ -209,8 +209,9 @@ engram_status run_chunks(const char *fn, HostPipe &hp, cudaStream_t s, int64_t T
 }
 
 // Device copies of the per-token host inputs (ids, positions, dead mask) of a
-// host-buffer call, carved from the front of its workspace, and the ids and
-// row ids the hash writes.
+// host-buffer call, carved from the front of its workspace, and the row ids the
+// hash writes (eids: room for compressed ids, which the one-launch
+// compress-hash does not need).
 struct HostIds {
   int32_t *ids, *positions, *eids, *rows;
   uint8_t *dead;

@@ -350,6 +350,7 @@ def test_compress_hash_argument_errors(eg):
     assert ch(e=C.c_void_p(0x10008)) == INV                # eids_out over the token ids
     assert ch(e=C.c_void_p(0x200010)) == INV               # eids_out over the row ids
     assert ch(out=C.c_void_p(0x10000)) == INV              # row ids over the token ids
+    assert ch(out=C.c_void_p(0x80040)) == INV              # row ids over the map
     assert ch(out=None) == INV
     bad = eg.engram_layout()
     bad._keep = (C.c_int64 * 6)(7, 11, 0, 13, 17, 19)
