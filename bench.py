@@ -747,14 +747,20 @@ def time_oracle(cfg, s, repeats=1):
 
 
 CONNECTION_CPU_SAMPLE = 4096
+CPU_BASELINE_SECONDS = 10.0   # about this much oracle work is timed (bounded)
 
 
 def cpu_baseline(cfg, d, n_tokens):
+    """The oracle's throughput on a bounded sample of the workload: one untimed
+    pass over the sample (warm-up, and its duration), then as many timed passes
+    as make about CPU_BASELINE_SECONDS of work (at most 100)."""
     import oracle
     if cfg.hidden:
         n_tokens = min(n_tokens, CONNECTION_CPU_SAMPLE)
     s = oracle_sample(cfg, d, n_tokens)
-    dt = time_oracle(cfg, s)
+    first = time_oracle(cfg, s)
+    passes = max(1, min(100, int(round(CPU_BASELINE_SECONDS / max(first, 1e-3)))))
+    dt = time_oracle(cfg, s, passes)
     what = ("compress + hash + connection (concatenated rows, wkv projection, gate, add)"
             if cfg.hidden else "compress + hash + fused lookup")
     where = "of sequence 0" if cfg.hidden else "(whole sequences)"
@@ -762,7 +768,8 @@ def cpu_baseline(cfg, d, n_tokens):
             "kind": "oracle",
             "sample": f"first {s['n']} tokens {where} of the {cfg.name} batch (same seeded "
                       f"inputs, the rows they need copied from the device): {what} in the fp64 "
-                      f"C oracle, {dt:.2f} s wall"}
+                      f"C oracle; {passes} timed passes after one untimed, "
+                      f"{dt * passes:.1f} s wall"}
 
 
 def reference_sample(cfg, n):
