@@ -23,8 +23,10 @@
  *
  * Conventions for every call:
  *  - Pointers named *_host are host memory; every other data pointer is device
- *    memory on the current CUDA device.  All memory is owned and allocated by the
- *    caller; the library allocates nothing and keeps no pointer after a call.
+ *    memory on the current CUDA device, except the members of engram_layout,
+ *    whose memory the struct's comment states per call.  All memory is owned
+ *    and allocated by the caller; the library allocates nothing and keeps no
+ *    pointer after a call.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream).  Calls are asynchronous on it; the library never synchronises
  *    except in engram_read_status.
