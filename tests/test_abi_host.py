@@ -359,3 +359,18 @@ def test_compress_hash_argument_errors(eg):
     assert ch(batch=0) == OK                              # nothing to do
     assert ch(seq=0, tok=None, out=None) == OK
 
+
+def test_plain_c_program_links_and_runs(eg, tmp_path):
+    """tests/c/engram_host_check.c, plain C99 against include/engram.h, links
+    against libengram.so and passes its host-only checks (version, strings, the
+    bucket draw's 462, argument errors, workspace sizes)."""
+    exe = tmp_path / "engram_host_check"
+    pkg = os.path.dirname(eg.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "engram_host_check.c"), "-o", str(exe),
+                    "-L", pkg, "-lengram", "-Wl,-rpath," + pkg],
+                   check=True, capture_output=True, text=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAIL" not in r.stdout and r.stdout.count("ok") >= 9
+
