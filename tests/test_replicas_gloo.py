@@ -60,7 +60,7 @@ def test_two_gloo_ranks_reassemble_the_batch():
     import workloads as W
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of this (threaded) process
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, join=True,
                        start_method="spawn")
