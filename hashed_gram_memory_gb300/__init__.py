@@ -286,7 +286,7 @@ def engram_compress_hash(token_ids, tid2eid, n_eids: int, n_heads: int, rows, hi
     _need(eids_out, (torch.int32,), "eids_out")
     _need(history, (torch.int32,), "history")
     _need(history_out, (torch.int32,), "history_out")
-    r = (C.c_int64 * 3)(*[int(x) for x in rows])
+    r = None if rows is None else (C.c_int64 * 3)(*[int(x) for x in rows])  # unused with primes
     lay = _layout(positions, dead, primes, host=False)
     _check(lib.engram_compress_hash(_ptr(token_ids), B, S, _ptr(tid2eid), tid2eid.numel(), n_eids,
                                     _ptr(history), _ptr(history_out), n_heads, r, _ref(lay),
