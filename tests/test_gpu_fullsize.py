@@ -1,9 +1,11 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark
-times (no aux outputs, out-of-place streams): tables and streams are generated on
-the GPU, token ids on the host.  Every compressed id and every row id is checked
-against the oracle; the streams are checked on a seeded sample of tokens, for
-which the oracle gets exactly the table rows and stream values the GPU read
-(copied back from the device: inputs, not results)."""
+times (engram_compress_hash then engram_lookup_fused, no aux outputs,
+out-of-place streams; a decode step as the one fused launch of engram_forward):
+tables and streams are generated on the GPU, token ids on the host.  Every
+compressed id and every row id is checked against the oracle; the streams are
+checked on a seeded sample of tokens, for which the oracle gets exactly the
+table rows and stream values the GPU read (copied back from the device: inputs,
+not results)."""
 import numpy as np
 import pytest
 
@@ -26,18 +28,32 @@ def eg():
 
 
 def run_full(eg, cfg, device_inputs):
-    """compress -> hash -> lookup exactly as bench.py launches them."""
+    """The step as bench.py launches it: engram_compress_hash (with the compressed
+    ids kept for the check) then engram_lookup_fused; a decode step's streams and
+    history come from engram_forward's fused launch, its ids from
+    engram_compress_hash."""
     import torch
     d = device_inputs
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    eids = eg.engram_compress(d["ids"], d["tid2eid"], cfg.n_eids, status=st, dead=d["dead"])
+    eids = torch.empty_like(d["ids"])
     hist_out = torch.empty_like(d["history"]) if d["history"] is not None else None
     primes = eg.engram_bucket_primes(1, 4, cfg.H, cfg.hash_vocab)[0] if cfg.hash_vocab else None
-    rows = eg.engram_hash(eids, cfg.H, cfg.rows, history=d["history"], history_out=hist_out,
-                          status=st, positions=d["positions"], primes=primes)
+    rows = eg.engram_compress_hash(d["ids"], d["tid2eid"], cfg.n_eids, cfg.H, cfg.rows,
+                                   history=d["history"], history_out=hist_out, eids_out=eids,
+                                   status=st, positions=d["positions"], dead=d["dead"],
+                                   primes=primes)
     out = torch.empty_like(d["streams"])
-    eg.engram_lookup_fused(rows, cfg.H, d["tables"], d["streams"], d["alpha"], cfg.eps,
-                           streams_out=out, status=st)
+    if cfg.decode:
+        hist_fused = torch.empty_like(d["history"])
+        eg.engram_forward(d["ids"], d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], d["streams"],
+                          d["alpha"], cfg.eps, history=d["history"], history_out=hist_fused,
+                          streams_out=out, status=st, positions=d["positions"], dead=d["dead"],
+                          primes=primes)
+        torch.cuda.synchronize()
+        assert torch.equal(hist_fused, hist_out)
+    else:
+        eg.engram_lookup_fused(rows, cfg.H, d["tables"], d["streams"], d["alpha"], cfg.eps,
+                               streams_out=out, status=st)
     code, flags = eg.engram_read_status(st)
     return eids, rows, hist_out, out, flags
 
