@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libengram.so")
 
-SOURCES = ["engram_api.cu", "compress_hash.cu", "lookup_fused.cu", "lookup_bulk.cu", "forward.cu",
-           "forward_static.cu", "wkv_gemm.cu", "connection.cu"]
+SOURCES = ["engram_api.cu", "compress_hash.cu", "lookup_fused.cu", "lookup_bulk.cu",
+           "decode_step.cu", "forward.cu", "forward_static.cu", "wkv_gemm.cu", "connection.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -71,7 +71,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static",
+    # -ldl: the NVTX ranges look up a profiler's injection library on first use
+    cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl",
                                                       "-Xcompiler", "-fvisibility=hidden"]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)

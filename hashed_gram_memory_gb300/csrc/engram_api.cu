@@ -105,6 +105,7 @@ ENGRAM_API engram_status engram_compress_masked(const int32_t *token_ids, int64_
                                                 int32_t n_eids, const uint8_t *dead,
                                                 int32_t *eids_out, int32_t *status,
                                                 void *stream) {
+  ENGRAM_NVTX_RANGE("engram_compress_masked");
   if (n_tokens < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_tokens < 0");
   if (vocab < 1) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: vocab < 1");
   if (n_eids < 0) return fail(ENGRAM_ERR_INVALID_ARG, "engram_compress: n_eids < 0");
@@ -129,6 +130,7 @@ ENGRAM_API engram_status engram_compress_masked(const int32_t *token_ids, int64_
 ENGRAM_API engram_status engram_compress(const int32_t *token_ids, int64_t n_tokens,
                                          const int32_t *tid2eid, int32_t vocab, int32_t n_eids,
                                          int32_t *eids_out, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_compress");
   return engram_compress_masked(token_ids, n_tokens, tid2eid, vocab, n_eids, nullptr, eids_out,
                                 status, stream);
 }
@@ -245,6 +247,7 @@ ENGRAM_API engram_status engram_hash_packed(const int32_t *eids, int32_t batch, 
                                             int32_t *history_out, int32_t n_heads,
                                             const int64_t *rows_host, int32_t *row_ids_out,
                                             int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_hash_packed");
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash: n_heads must be in [1, %d]",
                 ENGRAM_MAX_HEADS);
@@ -267,6 +270,7 @@ ENGRAM_API engram_status engram_hash_bucketed(const int32_t *eids, int32_t batch
                                               int32_t *history_out, int32_t n_heads,
                                               const int64_t *primes_host, int32_t *row_ids_out,
                                               int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_hash_bucketed");
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_hash_bucketed: n_heads must be in [1, %d]",
                 ENGRAM_MAX_HEADS);
@@ -291,6 +295,7 @@ ENGRAM_API engram_status engram_compress_hash(
     int32_t n_eids, const int32_t *history, int32_t *history_out, int32_t n_heads,
     const int64_t *rows_host, const engram_layout *layout_host, int32_t *eids_out,
     int32_t *row_ids_out, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_compress_hash");
   const char *fn = "engram_compress_hash";
   if (n_heads < 1 || n_heads > ENGRAM_MAX_HEADS)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
@@ -355,6 +360,7 @@ ENGRAM_API engram_status engram_hash(const int32_t *eids, int32_t batch, int32_t
                                      const int32_t *history, int32_t *history_out,
                                      int32_t n_heads, const int64_t *rows_host,
                                      int32_t *row_ids_out, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_hash");
   return engram_hash_packed(eids, batch, seq, nullptr, history, history_out, n_heads, rows_host,
                             row_ids_out, status, stream);
 }
@@ -457,6 +463,7 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
                                              const uint16_t *streams_in, uint16_t *streams_out,
                                              const float *alpha, float eps, float *gate_out,
                                              float *mem_out, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_lookup_fused");
   engram::LookupParams p;
   engram_status st =
       engram::prepare_lookup("engram_lookup_fused", row_ids, true, n_tokens, n_heads, tables_host,
@@ -540,6 +547,7 @@ ENGRAM_API engram_status engram_concat_rows(const int32_t *row_ids, int64_t n_to
                                             int32_t n_heads, const engram_tables *tables_host,
                                             uint16_t *e_out, uint8_t *state_out, int32_t *status,
                                             void *stream) {
+  ENGRAM_NVTX_RANGE("engram_concat_rows");
   const char *fn = "engram_concat_rows";
   if (n_tokens < 0 || n_tokens > INT32_MAX)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
@@ -558,6 +566,7 @@ ENGRAM_API engram_status engram_concat_rows(const int32_t *row_ids, int64_t n_to
 ENGRAM_API engram_status engram_wkv_project(const uint16_t *e, int64_t n_tokens, int32_t K,
                                             const uint16_t *wkv, int32_t D, float *k_out,
                                             int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_wkv_project");
   const char *fn = "engram_wkv_project";
   if (n_tokens < 0 || n_tokens > INT32_MAX)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
@@ -579,6 +588,7 @@ ENGRAM_API engram_status engram_gate_add(const float *k, const uint8_t *state, i
                                          int32_t D, const uint16_t *streams_in,
                                          uint16_t *streams_out, const float *alpha, float eps,
                                          float *gate_out, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_gate_add");
   const char *fn = "engram_gate_add";
   if (n_tokens < 0 || n_tokens > INT32_MAX)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
@@ -602,6 +612,7 @@ ENGRAM_API engram_status engram_connection(const int32_t *row_ids, int64_t n_tok
                                            const float *alpha, float eps, void *workspace,
                                            size_t workspace_bytes, float *gate_out, float *k_out,
                                            int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_connection");
   const char *fn = "engram_connection";
   if (n_tokens < 0 || n_tokens > INT32_MAX)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_tokens out of range", fn);
@@ -659,6 +670,7 @@ ENGRAM_API void engram_debug_withhold_copies(int32_t launches) {
 
 ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flags_host,
                                             void *stream) {
+  ENGRAM_NVTX_RANGE("engram_read_status");
   if (!status || !flags_host)
     return fail(ENGRAM_ERR_INVALID_ARG, "engram_read_status: NULL pointer");
   int32_t v = 0;

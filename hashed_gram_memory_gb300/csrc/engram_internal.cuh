@@ -4,11 +4,23 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "engram.h"
 
 namespace engram {
+
+// A named NVTX range over a C-ABI call, so that a profiler's timeline shows
+// each call and the kernels it launched; without a profiler attached the push
+// and pop return at once.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define ENGRAM_NVTX_RANGE(name) const ::engram::NvtxRange engram_nvtx_range_(name)
 
 constexpr int kMaxHeads = ENGRAM_MAX_HEADS;
 constexpr int kMaxRows = 3 * kMaxHeads;
@@ -93,6 +105,7 @@ cudaError_t launch_hash(const HashParams &p, cudaStream_t stream);
 cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_supported(int D, int dtype, int H);
+size_t bulk_smem_bytes(int D, int dtype, int H);  // one token's rows, scales and barrier
 cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk_small(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_small_supported(int D, int dtype, int H);
@@ -118,6 +131,9 @@ engram_status prepare_lookup(const char *fn, const int32_t *row_ids, bool need_r
                              float eps, float *gate_out, float *mem_out, int32_t *status,
                              LookupParams &p);
 int lookup_kernel_choice();
+// engram_forward runs this call as the fused decode launch (no workspace used).
+bool forward_is_decode_step(int32_t batch, int32_t seq, int32_t n_heads,
+                            const engram_tables *tables_host);
 
 // Records the message engram_last_error() returns on this thread; returns code.
 engram_status set_error(engram_status code, const char *fmt, ...);

@@ -161,6 +161,20 @@ engram_status decode_step(const int32_t *token_ids, int32_t batch, const int32_t
 
 }  // namespace
 
+namespace engram {
+
+// One new token a slot, and the bulk lookup family applies: engram_forward runs
+// the step as the one fused decode launch, which needs no workspace.
+bool forward_is_decode_step(int32_t batch, int32_t seq, int32_t n_heads,
+                            const engram_tables *tables_host) {
+  if (seq != 1 || batch < 1 || !tables_host) return false;
+  const int which = lookup_kernel_choice();
+  return (which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
+         bulk_supported(tables_host->D, tables_host->dtype, n_heads);
+}
+
+}  // namespace engram
+
 namespace {
 
 // The chunk pipeline of the host-buffer calls.  Chunk c of the streams uses
@@ -307,6 +321,7 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
                                         const uint16_t *streams_in, uint16_t *streams_out,
                                         const float *alpha, float eps, void *workspace,
                                         size_t workspace_bytes, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_forward");
   if (batch < 0 || seq < 0 || n_heads < 1 || n_heads > ENGRAM_MAX_HEADS || !tables_host)
     return fwd_fail(ENGRAM_ERR_INVALID_ARG, "engram_forward: bad sizes or NULL tables");
   const size_t need = engram_forward_workspace_bytes(batch, seq, n_heads);
@@ -318,14 +333,10 @@ ENGRAM_API engram_status engram_forward(const int32_t *token_ids, int32_t batch,
   uint64_t mod[3][engram::kMaxHeads], off[3][engram::kMaxHeads];
   engram_status st = layout_buckets("engram_forward", tables_host, layout_host, n_heads, mod, off);
   if (st != ENGRAM_OK) return st;
-  if (seq == 1 && T > 0) {
-    const int which = engram::lookup_kernel_choice();
-    if ((which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
-        engram::bulk_supported(tables_host->D, tables_host->dtype, n_heads))
-      return decode_step(token_ids, batch, tid2eid, vocab, n_eids, history, history_out, n_heads,
-                         tables_host, layout_host, streams_in, streams_out, alpha, eps, status,
-                         stream);
-  }
+  if (engram::forward_is_decode_step(batch, seq, n_heads, tables_host))
+    return decode_step(token_ids, batch, tid2eid, vocab, n_eids, history, history_out, n_heads,
+                       tables_host, layout_host, streams_in, streams_out, alpha, eps, status,
+                       stream);
   int32_t *rows = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + round_up(T * 4));
   st = ids_to_rows(token_ids, batch, seq, tid2eid, vocab, n_eids, history,
                    history_out, n_heads, tables_host,
@@ -353,6 +364,7 @@ ENGRAM_API engram_status engram_forward_host(
     const engram_tables *tables_host, const engram_layout *layout_host,
     const uint16_t *streams_in_host, uint16_t *streams_out_host, const float *alpha, float eps,
     int32_t chunk_tokens, void *workspace, size_t workspace_bytes, int32_t *status, void *stream) {
+  ENGRAM_NVTX_RANGE("engram_forward_host");
   const char *fn = "engram_forward_host";
   if (!tables_host || batch < 0 || seq < 0 || n_heads < 1 || n_heads > ENGRAM_MAX_HEADS ||
       chunk_tokens < 0)
@@ -444,6 +456,7 @@ ENGRAM_API engram_status engram_connection_host(
     int32_t D, const uint16_t *streams_in_host, uint16_t *streams_out_host, const float *alpha,
     float eps, int32_t chunk_tokens, void *workspace, size_t workspace_bytes, int32_t *status,
     void *stream) {
+  ENGRAM_NVTX_RANGE("engram_connection_host");
   const char *fn = "engram_connection_host";
   if (!tables_host || batch < 0 || seq < 0 || n_heads < 1 || n_heads > ENGRAM_MAX_HEADS ||
       chunk_tokens < 0 || D < 1)

@@ -24,337 +24,19 @@
 // is copied; a dead token (all ids ENGRAM_ROW_DEAD) copies its streams through.
 #include <atomic>
 
+#include "bulk_copy.cuh"
+#include "bulk_token.cuh"
 #include "engram_internal.cuh"
-#include "hash_device.cuh"
 #include "lookup_common.cuh"
 
 namespace engram {
 namespace {
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// 1-D bulk copy global -> this CTA's shared memory, completing `bytes` on `bar`.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Asks L2 to fetch `bytes` (a multiple of 16) at `src` (16-byte aligned) ahead of use.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Polls the phase with parity 0 of `bar` until it completes (true) or limit_ns
-// passes (false).
-__device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns) {
-  if (mbar_try_wait(bar, 0)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, 0)) return true;
-    if ((int64_t)(global_ns() - t0) > limit_ns) return false;
-  }
-}
-
-// EARLY: the stream slices are loaded into registers before the rows arrive
-// (two blocks per SM); otherwise after them, keeping the block within 64
-// registers per thread so that four blocks share an SM (small tokens).
-// Token t of a one-token-a-block launch, its 3H row ids at `ids` (global or
-// shared memory).
-template <int DT, bool AUX, bool EARLY>
-__device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t *ids,
-                                           const int64_t t) {
-  constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;                // FP8 bytes
-  constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
-  constexpr int kElt = kFp8 ? 1 : 2;
-  extern __shared__ __align__(128) uint8_t sm[];
-
-  const int H = p.H, R = 3 * H, D = p.D;
-  const uint32_t row_bytes = (uint32_t)D * kElt;
-  const uint32_t exp_bytes = kE8 ? (uint32_t)D / 32 : 0;         // a row's block exponents
-  uint8_t *s_rows = sm;                                          // [R][row_bytes]
-  uint8_t *s_exps = s_rows + (size_t)R * row_bytes;              // [R][exp_bytes]
-  uint64_t *bar = reinterpret_cast<uint64_t *>(s_exps + (size_t)R * exp_bytes);
-  float *s_scale = reinterpret_cast<float *>(bar + 1);           // [R]
-  float *s_red = s_scale + kMaxRows;                             // [8][3]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int col0 = tid * 16;
-
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  // Range checks: thread r looks at row r (a loop when the block is narrower).
-  bool bad_here = false, dead_here = false, live_here = false;
-  for (int r = tid; r < R; r += blockDim.x) {
-    const int ni = (r >= H) + (r >= 2 * H);
-    const int32_t id = ids[r];
-    if (id == ENGRAM_ROW_DEAD) {
-      dead_here = true;
-    } else {
-      live_here = true;
-      bad_here |= (id < 0) | ((int64_t)id >= p.rows[ni]);
-    }
-  }
-  if (__syncthreads_or(bad_here || dead_here)) {
-    // A token whose ids are all dead passes through; any other mix is bad.
-    if (__syncthreads_and(!live_here)) {
-      pass_through16(p.x + t * 4 * D + col0, p.y + t * 4 * D + col0, D,
-                     AUX && p.gate_out ? p.gate_out + t : nullptr,
-                     AUX && p.mem_out ? p.mem_out + t * D + col0 : nullptr, tid == 0);
-    } else if (tid == 0 && p.status) {
-      atomicOr(p.status, ENGRAM_FLAG_BAD_ROW);
-    }
-    return;  // whole block: nothing issued
-  }
-
-  // Warp 0: every row copy of the token on the one barrier, lane r issuing the
-  // copies of rows r, r + 32, r + 64 from ids it loads itself (in parallel).
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)R * row_bytes);
-    __syncwarp();
-    const int withheld = p.withhold != 0 ? 0 : -1;  // test hook: row 0's copy is never issued
-    for (int r = lane; r < R; r += 32) {
-      const int ni = (r >= H) + (r >= 2 * H);
-      const int64_t id = ids[r];
-      if (r != withheld)
-        bulk_g2s(s_rows + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
-    }
-    // Streams read after the rows: their HBM reads start now, under the row
-    // copies, and the loads below find them in L2.
-    if (!EARLY && lane == 0) prefetch_l2(p.x + t * 4 * D, (uint32_t)(8 * D));
-  }
-  // Meanwhile: the row scales into shared memory, the stream slices into registers.
-  if constexpr (kE8) {
-    // The rows' block exponents (D/32 bytes each, a multiple of 16 here), 16
-    // bytes per thread, coalesced: their latency overlaps the row copies.
-    const int per_row = (int)exp_bytes / 16;
-    for (int i = tid; i < R * per_row; i += blockDim.x) {
-      const int r = i / per_row, c = i - r * per_row;
-      const int ni = (r >= H) + (r >= 2 * H);
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-          static_cast<const uint8_t *>(p.scale[ni]) + (int64_t)ids[r] * exp_bytes) + c);
-      *reinterpret_cast<uint4 *>(s_exps + (size_t)r * exp_bytes + 16 * c) = v;
-    }
-  }
-  // fp32 row scales: thread r loads row r's scale; with the streams loaded
-  // early it stores the scale only after issuing them (a store waits for its
-  // load, and the stream loads should not wait behind it: 0.952 -> 0.961 on
-  // the 8-head prefill; the same order for the e8m0 exponents measured 0.921 ->
-  // 0.914, so they keep theirs).
-  float sc = 0.f;
-  if (kFp8 && !kE8 && tid < R) {
-    const int ni = (tid >= H) + (tid >= 2 * H);
-    sc = __ldg(static_cast<const float *>(p.scale[ni]) + ids[tid]);
-    if (!EARLY) s_scale[tid] = sc;
-  }
-  uint4 xs[4][2];
-  const uint16_t *xrow = p.x + t * 4 * D + col0;
-  if (EARLY) {
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
-      xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
-    }
-  }
-  if (kFp8 && !kE8) {
-    if (EARLY && tid < R) s_scale[tid] = sc;
-    for (int r = tid + blockDim.x; r < R; r += blockDim.x) {
-      const int ni = (r >= H) + (r >= 2 * H);
-      s_scale[r] = __ldg(static_cast<const float *>(p.scale[ni]) + ids[r]);
-    }
-  }
-
-  const bool landed = wait_bounded(bar, p.wait_limit_ns);
-  // Block-uniform outcome (every wait above is bounded, so all threads get here);
-  // the barrier also publishes the scales.
-  if (__syncthreads_or(!landed)) {
-    if (tid == 0) {
-      if (p.status) atomicOr(p.status, ENGRAM_FLAG_TIMEOUT);
-      wait_bounded(bar, p.wait_limit_ns);  // let the issued copies land before exit
-    }
-    return;
-  }
-
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  const uint8_t *src = s_rows + (size_t)col0 * kElt;
-#pragma unroll 4
-  for (int r = 0; r < R; ++r) {
-    const uint8_t *row = src + (size_t)r * row_bytes;
-    if (kFp8) {
-      const float scale = kE8 ? e8m0_to_float(s_exps[(size_t)r * exp_bytes + (col0 >> 5)]) : s_scale[r];
-      acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), scale);
-    } else {
-      acc_bf16(acc, *reinterpret_cast<const uint4 *>(row));
-      acc_bf16(acc + 8, *reinterpret_cast<const uint4 *>(row + 16));
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] *= p.inv_R;
-
-  if (!EARLY) {
-    xs[0][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow));
-    xs[0][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + 8));
-  }
-  float saa = 0.f, smm = 0.f, sam = 0.f;
-  gate_partials(xs[0][0], xs[0][1], acc, saa, smm, sam);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    saa += __shfl_xor_sync(0xffffffffu, saa, o);
-    smm += __shfl_xor_sync(0xffffffffu, smm, o);
-    sam += __shfl_xor_sync(0xffffffffu, sam, o);
-  }
-  if (lane == 0) {
-    s_red[3 * warp + 0] = saa;
-    s_red[3 * warp + 1] = smm;
-    s_red[3 * warp + 2] = sam;
-  }
-  __syncthreads();
-  const int nw = blockDim.x >> 5;
-  saa = smm = sam = 0.f;
-  for (int w = 0; w < nw; ++w) {
-    saa += s_red[3 * w + 0];
-    smm += s_red[3 * w + 1];
-    sam += s_red[3 * w + 2];
-  }
-  const float g = gate_value(saa, smm, sam, (float)D, p.eps, p.sqrt_D);
-
-  uint16_t *yrow = p.y + t * 4 * D + col0;
-#pragma unroll
-  for (int s = 0; s < 4; ++s) {
-    if (!EARLY && s > 0) {
-      xs[s][0] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D));
-      xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
-    }
-    const float c = g * __ldg(p.alpha + s);
-    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D), gated_add8(xs[s][0], acc, c));
-    __stcs(reinterpret_cast<uint4 *>(yrow + (int64_t)s * D + 8), gated_add8(xs[s][1], acc + 8, c));
-  }
-  if (AUX) {
-    if (p.gate_out && tid == 0) p.gate_out[t] = g;
-    if (p.mem_out) {
-      float4 *mo = reinterpret_cast<float4 *>(p.mem_out + t * D + col0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        mo[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-    }
-  }
-}
 
 template <int DT, bool AUX, bool EARLY>
 __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
     lookup_bulk_kernel(const __grid_constant__ LookupParams p) {
   const int64_t t = blockIdx.x;
   bulk_token<DT, AUX, EARLY>(p, p.row_ids + t * 3 * p.H, t);
-}
-
-// The decode step in one launch (one new token per slot, one slot a block):
-// thread 0 compresses the slot's token id (a slot of the dead mask becomes the
-// dead id), builds its window from the slot's history (the pad id 0 without
-// one) back to its lookback limit (its position in its sample when positions
-// are given), and writes the updated history; the first 3H threads hash the
-// window into the row ids (the hash kernel's arithmetic, hash_device.cuh; a
-// dead slot gets ENGRAM_ROW_DEAD), kept in shared memory; then the block looks
-// them up as bulk_token does.  A bad token id, map value or history id flags
-// the status word and leaves all of the slot's outputs unwritten.
-template <int DT, bool AUX, bool EARLY>
-__global__ void __launch_bounds__(256, EARLY ? 2 : 4)
-    decode_step_kernel(const __grid_constant__ DecodeParams p) {
-  __shared__ int32_t s_ids[kMaxRows];
-  __shared__ int32_t s_win[4];
-  __shared__ int s_skip, s_dead;
-  const int64_t b = blockIdx.x;
-  const int H = p.lk.H, R = 3 * H;
-  // The slot's streams do not depend on its token: their HBM reads start now,
-  // under the dependent loads of the token and its map entry.
-  if (threadIdx.x == 32) prefetch_l2(p.lk.x + b * 4 * p.lk.D, (uint32_t)(8 * p.lk.D));
-  if (threadIdx.x == 0) {
-    int32_t raw[3] = {0, 0, 0};
-    if (p.history)
-      for (int k = 0; k < 3; ++k) raw[k] = p.history[b * 3 + k];
-    // A dead slot compresses to the dead id whatever its token (no range check).
-    const bool dead = p.dead && p.dead[b];
-    uint32_t flag = 0;
-    int32_t e = ENGRAM_EID_DEAD, w[4];
-    if (!dead) {
-      const int32_t tok = p.token_ids[b];
-      if ((uint32_t)tok >= (uint32_t)p.vocab) {
-        flag = ENGRAM_FLAG_BAD_TOKEN;
-      } else {
-        e = __ldg(p.tid2eid + tok);
-        if (e < 0 || e > p.n_eids) flag = ENGRAM_FLAG_BAD_EID;
-      }
-      // lookback: the position in the sample if given, else the 3-id history or nothing
-      const int64_t limit = p.positions ? (int64_t)p.positions[b] : (p.history ? 3 : 0);
-      if (!flag && !make_window(raw, e, limit, w)) flag = ENGRAM_FLAG_BAD_EID;
-    }
-    if (!flag) {
-      if (!dead)
-        for (int k = 0; k < 4; ++k) s_win[k] = w[k];
-      if (p.history_out) {
-        p.history_out[b * 3 + 0] = raw[1];
-        p.history_out[b * 3 + 1] = raw[2];
-        p.history_out[b * 3 + 2] = e;
-      }
-    } else if (p.lk.status) {
-      atomicOr(p.lk.status, (int32_t)flag);
-    }
-    s_skip = flag != 0;
-    s_dead = dead;
-  }
-  __syncthreads();
-  if (s_skip) return;  // block-uniform
-  for (int r = threadIdx.x; r < R; r += blockDim.x) {
-    int32_t id = ENGRAM_ROW_DEAD;
-    if (!s_dead) {
-      const int32_t w[4] = {s_win[0], s_win[1], s_win[2], s_win[3]};
-      id = window_row(w, r, H, p.seed, p.mod, p.rmul, p.off);
-    }
-    s_ids[r] = id;
-    if (p.row_ids_out) p.row_ids_out[b * R + r] = id;
-  }
-  __syncthreads();
-  bulk_token<DT, AUX, EARLY>(p.lk, s_ids, b);
 }
 
 // A row's e8m0 exponents, n = D/32 bytes with n in {1, 2, 4, 8} (the small-row
@@ -554,25 +236,6 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
-// Raises a kernel's dynamic shared-memory ceiling, once per device, to the 227 KB
-// a block may use less the kernel's static shared memory (any launch's request
-// fits under it).  `configured` is the kernel's own bit set of devices done.
-template <typename Kernel>
-cudaError_t raise_smem_ceiling(Kernel kern, std::atomic<uint64_t> &configured) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kern);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(227 * 1024 - fa.sharedSizeBytes));
-  if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_release);
-  return e;
-}
-
 template <int DT, bool AUX, bool EARLY>
 cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t stream) {
   auto kern = lookup_bulk_kernel<DT, AUX, EARLY>;
@@ -581,26 +244,6 @@ cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t strea
   if (e != cudaSuccess) return e;
   kern<<<(unsigned)p.T, p.D / 16, smem, stream>>>(p);
   return cudaGetLastError();
-}
-
-template <int DT, bool AUX, bool EARLY>
-cudaError_t launch_decode_t(const DecodeParams &p, size_t smem, cudaStream_t stream) {
-  auto kern = decode_step_kernel<DT, AUX, EARLY>;
-  static std::atomic<uint64_t> configured{0};
-  const cudaError_t e = raise_smem_ceiling(kern, configured);
-  if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.lk.T, p.lk.D / 16, smem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-template <int DT>
-cudaError_t launch_decode_dt(const DecodeParams &p, size_t smem, bool aux, bool early,
-                             cudaStream_t stream) {
-  if (early)
-    return aux ? launch_decode_t<DT, true, true>(p, smem, stream)
-               : launch_decode_t<DT, false, true>(p, smem, stream);
-  return aux ? launch_decode_t<DT, true, false>(p, smem, stream)
-             : launch_decode_t<DT, false, false>(p, smem, stream);
 }
 
 template <int DT>
@@ -687,18 +330,6 @@ size_t bulk_smem_bytes(int D, int dtype, int H) {
 bool bulk_supported(int D, int dtype, int H) {
   return D % 512 == 0 && D >= 512 && D <= ENGRAM_MAX_D &&
          bulk_smem_bytes(D, dtype, H) <= 227 * 1024;
-}
-
-cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream) {
-  if (p.lk.T == 0) return cudaSuccess;
-  const size_t smem = bulk_smem_bytes(p.lk.D, dtype, p.lk.H);
-  const bool aux = p.lk.gate_out != nullptr || p.lk.mem_out != nullptr;
-  const bool early = smem > 56 * 1024;
-  if (dtype == ENGRAM_TABLE_FP8_E4M3FN)
-    return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
-  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
-    return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32>(p, smem, aux, early, stream);
-  return launch_decode_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream) {

@@ -459,18 +459,28 @@ ENGRAM_API engram_status engram_connection_host(
  * calling convenience.
  *
  * Instead of a caller workspace it uses one file-scope device array of
- * ENGRAM_STATIC_WORKSPACE_BYTES (16 MiB), which every device that loads the
- * library holds until the process exits.  The call allocates nothing: no
- * cudaMalloc, no cudaFree, no allocating library routine.  Its first call on a
- * device looks up the array's device address there (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture.
+ * ENGRAM_STATIC_WORKSPACE_BYTES (16 MiB).  A device reserves it when the
+ * library's code is loaded there, at the latest on the first call of this
+ * function on that device (with lazy module loading, CUDA's default), and holds
+ * it until the process exits; a first call can therefore fail with
+ * ENGRAM_ERR_CUDA when the device is out of memory.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.  Outside
+ * a stream capture every call looks up the array's device address
+ * (cudaGetSymbolAddress, with the calling device current), so a context made
+ * anew after cudaDeviceReset gets its own; a call inside a capture reuses the
+ * address the last call outside one found on that device, and returns
+ * ENGRAM_ERR_INVALID_ARG if there was none.  So make one call per device at
+ * start-up, outside any capture, and again after a device reset: a call with
+ * batch = 0 or seq = 0 does the set-up and launches nothing.
  * Requests needing more than the array, engram_forward_workspace_bytes(batch,
- * seq, n_heads) > ENGRAM_STATIC_WORKSPACE_BYTES (about 160K tokens at 8 heads),
- * return ENGRAM_ERR_UNSUPPORTED with a message and launch nothing.  All calls
- * share the one array, which keeps the last call's contents; each call clears
- * the part it uses on `stream` first.  Calls that overlap on the GPU (on
- * different streams or host threads, on one device) race on the array: order
- * them.  Other arguments and results are exactly those of engram_forward.
+ * seq, n_heads) > ENGRAM_STATIC_WORKSPACE_BYTES (100 bytes a token at 8 heads:
+ * 167,772 tokens), return ENGRAM_ERR_UNSUPPORTED with a message and launch
+ * nothing.  All calls share the one array, which keeps the last call's
+ * contents; each call that uses it clears the part it uses on `stream` first (a
+ * decode step, seq = 1 on the fused launch, keeps its ids on chip and uses none
+ * of it).  Calls that overlap on the GPU (on different streams or host threads,
+ * on one device) race on the array: order them.  Other arguments and results
+ * are exactly those of engram_forward.
  */
 #define ENGRAM_STATIC_WORKSPACE_BYTES (16u << 20)
 ENGRAM_API engram_status engram_forward_static(
