@@ -1,18 +1,21 @@
 """Benchmark of the Engram hashed n-gram memory lookup on GB300.
 
 One step = the whole hot path over one batch through the C ABI:
-engram_compress_hash (compression and hash in one launch) -> engram_lookup_fused.  The default workload is the mid-size
-prefill (batch 4 x seq 4096 tokens, Zipf token ids, 4 hash heads, 4096-wide
-rows, three 1,000,000-row FP8 e4m3fn tables with fp32 row scales = 12.3 GB, bf16
-streams [4, 4096, 4, 4096]); --workload picks another (workloads.py: the
-full-size prefill of 65,536 tokens over 57.7 GiB of tables, a 512-slot decode
-step, BF16 tables, packed batches, e8m0 block scales, the released bucket
-layout, the wkv connection).  Inputs are resident in HBM when the timed region
-starts, larger than the 129 MB L2, or rotated among buffers when a step's
-streams fit in it.  The K timed steps are captured once into
-a CUDA graph and replayed (--eager launches them one by one from Python); CUDA
-events recorded inside the graph time the dominant kernel.  Prints ONE JSON
-line (rank 0).
+engram_compress_hash (compression and hash in one launch) -> engram_lookup_fused.
+The default workload is the full-size prefill (batch 8 x seq 8192 = 65,536
+tokens, Zipf token ids with 5 % of positions copying an earlier 4-token span, 8
+hash heads, three 5,040,000-row FP8 e4m3fn tables of 4096-wide rows with fp32 row
+scales = 57.7 GiB, bf16 streams [8, 8192, 4, 4096]), the largest configuration
+that fits one GPU; --workload picks another (workloads.py: the mid-size prefill,
+a 512-slot decode step, BF16 tables, packed batches, e8m0 block scales, the
+released bucket layout, the wkv connection).  Inputs are resident in HBM when
+the timed region starts, larger than the 129 MB L2, or rotated among buffers
+when a step's streams fit in it.  The K timed steps are captured once into a
+CUDA graph (--eager launches them one by one from Python); the timed region
+replays that graph back to back until it has lasted at least a second (so the
+clock samples taken every 100 ms cover it), each replay of exactly K steps
+between CUDA events, and reports the median replay.  CUDA events recorded
+inside a second graph time the dominant kernel.  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -39,10 +42,14 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "mid_prefill_fp8"
+DEFAULT_WORKLOAD = "full_prefill_fp8"
 METRIC = "Engram fused lookup tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lookup_fused_traffic.json")
+# The timed region replays the K steps until it has lasted this long, so that the
+# clock sampler (one sample every 100 ms) sees it; at most MAX_REPLAYS replays.
+MIN_TIMED_S = 1.0
+MAX_REPLAYS = 20000
 
 
 def parse():
@@ -68,7 +75,18 @@ def parse():
                     help="override the bucketed layout's hash vocabulary (the table shrinks to "
                          "the sum of its buckets; small cases for ncu captures)")
     ap.add_argument("--lookup-kernel", default="auto", choices=["auto", "gather", "bulk"])
+    ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
+                    help="replay the K timed steps until the timed region lasts this long")
     return ap.parse_args()
+
+
+def replays_for(replay_s: float, min_timed_s: float = MIN_TIMED_S) -> int:
+    """How many back-to-back replays of the K steps make a timed region of at
+    least min_timed_s, given one replay's duration (at least one, at most
+    MAX_REPLAYS)."""
+    if replay_s <= 0:
+        return 1
+    return int(max(1, min(MAX_REPLAYS, -(-min_timed_s // replay_s))))
 
 
 def config_of(name: str, args=None) -> W.EngramConfig:
@@ -87,11 +105,20 @@ def config_of(name: str, args=None) -> W.EngramConfig:
 L2_BYTES = 126 * 2**20   # GB300 L2
 
 
+def step_footprint(cfg: W.EngramConfig) -> int:
+    """Bytes a step reads or writes that could stay in L2 from one step to the next:
+    the streams in and out, and the table rows (with their scales) its tokens
+    select, counted as if every row were distinct."""
+    return cfg.T * 4 * cfg.width * 2 * 2 + cfg.T * cfg.R * cfg.row_bytes()
+
+
 def stream_rotation(cfg: W.EngramConfig, l2_bytes: int = L2_BYTES) -> int:
-    """How many separate stream buffers the timed steps cycle through, so that a
-    step never finds its input streams in L2: one when a step's streams (in +
-    out) already exceed twice the L2, else enough copies to exceed it."""
-    per_step = cfg.T * 4 * cfg.width * 2 * 2
+    """How many separate input sets (token ids, history, streams in and out) the
+    timed steps cycle through, so that a step finds neither its streams nor its
+    table rows in L2: one when a step's footprint already exceeds twice the L2,
+    else enough sets to exceed it.  Each set has its own token ids, so its rows
+    are other rows of the tables."""
+    per_step = step_footprint(cfg)
     if per_step >= 2 * l2_bytes:
         return 1
     return min(256, -(-2 * l2_bytes // per_step))
@@ -99,15 +126,18 @@ def stream_rotation(cfg: W.EngramConfig, l2_bytes: int = L2_BYTES) -> int:
 
 def l2_note(cfg: W.EngramConfig, l2_bytes: int = L2_BYTES) -> str:
     per_step = cfg.T * 4 * cfg.width * 2
+    rows = cfg.T * cfg.R * cfg.row_bytes()
     n = stream_rotation(cfg, l2_bytes)
     if n == 1:
         return (f"no flush: every input is larger than the {l2_bytes / 2**20:.0f} MiB L2 (tables "
-                f"{cfg.table_bytes() / 2**30:.1f} GiB; streams {per_step / 1e9:.3f} GB read and "
+                f"{cfg.table_bytes() / 2**30:.1f} GiB, of which a step gathers "
+                f"{rows / 1e9:.3f} GB of rows; streams {per_step / 1e9:.3f} GB read and "
                 f"{per_step / 1e9:.3f} GB written per step)")
-    return (f"inputs larger than L2 by rotation: the streams of a step ({per_step / 1e6:.1f} MB "
-            f"read, as many written) fit in the {l2_bytes / 2**20:.0f} MiB L2, so the timed steps cycle "
-            f"through {n} separate input and output buffers ({2 * n * per_step / 1e6:.0f} MB); "
-            f"tables {cfg.table_bytes() / 2**30:.1f} GiB")
+    return (f"inputs larger than L2 by rotation: a step's streams ({per_step / 1e6:.1f} MB read, as "
+            f"many written) and the rows its tokens gather ({rows / 1e6:.1f} MB) fit in the "
+            f"{l2_bytes / 2**20:.0f} MiB L2, so the timed steps cycle through {n} separate sets of "
+            f"token ids, history, input and output streams ({n * step_footprint(cfg) / 1e6:.0f} MB "
+            f"with their rows); tables {cfg.table_bytes() / 2**30:.1f} GiB")
 
 
 def workload_desc(cfg: W.EngramConfig) -> dict:
@@ -292,16 +322,17 @@ class Step:
             self.k = torch.empty((cfg.T, cfg.hidden), dtype=torch.float32, device=dev)
             self.launches = 4
 
-    def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None):
+    def __call__(self, ev_start=None, ev_end=None, ids=None, x=None, out=None, hist=None):
         eg, cfg, d = self.eg, self.cfg, self.d
         ids = d["ids"] if ids is None else ids
+        hist = d["history"] if hist is None else hist
         x = d["streams"] if x is None else x
         out = self.out if out is None else out
         if self.fused_decode:
             if ev_start is not None:
                 ev_start.record(self.stream)
             eg.engram_forward(ids, d["tid2eid"], cfg.n_eids, cfg.H, d["tables"], x, d["alpha"],
-                              cfg.eps, history=d["history"], history_out=self.hist_out,
+                              cfg.eps, history=hist, history_out=self.hist_out,
                               streams_out=out, workspace=self.ws, status=self.status,
                               stream=self.stream, positions=d["positions"], dead=d["dead"],
                               primes=self.primes)
@@ -309,7 +340,7 @@ class Step:
                 ev_end.record(self.stream)
             return
         eg.engram_compress_hash(ids, d["tid2eid"], cfg.n_eids, cfg.H, cfg.rows,
-                                history=d["history"], history_out=self.hist_out,
+                                history=hist, history_out=self.hist_out,
                                 row_ids_out=self.rows, status=self.status, stream=self.stream,
                                 positions=d["positions"], dead=d["dead"], primes=self.primes)
         if cfg.hidden:
@@ -383,10 +414,22 @@ def run_native(args):
         raise SystemExit(f"device status flags 0x{flags:x} during warm-up")
 
     K = args.steps
-    # Streams that fit in L2 rotate among separate buffers (see stream_rotation).
+    # A step whose streams and rows fit in L2 rotates among separate input sets
+    # (see stream_rotation): set 0 is the workload's own; set k > 0 has token ids
+    # and history drawn as replica rank * 1000 + k draws them, so its rows are
+    # others.
     n_rot = stream_rotation(cfg)
     xs_rot = [d["streams"]] + [d["streams"].clone() for _ in range(n_rot - 1)]
     ys_rot = [step.out] + [torch.empty_like(step.out) for _ in range(n_rot - 1)]
+    ids_rot = [d["ids"]] + [torch.from_numpy(W.token_ids(cfg, rank * 1000 + k)).to(device)
+                            for k in range(1, n_rot)]
+    hist_rot = [d["history"]] + [None if d["history"] is None else
+                                 torch.from_numpy(W.history(cfg, rank * 1000 + k)).to(device)
+                                 for k in range(1, n_rot)]
+
+    def rot(i):
+        k = i % n_rot
+        return dict(x=xs_rot[k], out=ys_rot[k], ids=ids_rot[k], hist=hist_rot[k])
     # The K timed steps are captured once into a CUDA graph and replayed, so the
     # GPU runs them back to back without waiting on Python between launches.
     # The step throughput comes from a graph of the K steps alone; the dominant
@@ -402,38 +445,55 @@ def run_native(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(K):
-                step(x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
+                step(**rot(i))
         graph_ev = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_ev, stream=stream):
             for i in range(K):
-                step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
+                step(ev[i][0], ev[i][1], **rot(i))
         with torch.cuda.stream(stream):
             graph.replay()       # untimed: a graph's first launch uploads it
             graph_ev.replay()
         torch.cuda.synchronize()
+
+    def run_k():
+        """Exactly K steps: one replay of the step graph, or K eager steps."""
+        if graphed:
+            with torch.cuda.stream(stream):
+                graph.replay()
+        else:
+            for i in range(K):
+                step(ev[i][0], ev[i][1], **rot(i))
+
+    # One untimed replay sizes the timed region: enough replays of the K steps
+    # to last MIN_TIMED_S.
+    t_begin.record(stream)
+    run_k()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    n_rep = replays_for(t_begin.elapsed_time(t_end) * 1e-3, args.min_timed_s)
+    if world > 1:   # every rank replays as often as rank 0
+        n_rep = int(max_over_ranks(float(n_rep), device))
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    t_begin.record(stream)
-    if graphed:
-        with torch.cuda.stream(stream):
-            graph.replay()
-    else:
-        for i in range(K):
-            step(ev[i][0], ev[i][1], x=xs_rot[i % n_rot], out=ys_rot[i % n_rot])
-    t_end.record(stream)
+    marks[0].record(stream)
+    for r in range(n_rep):
+        run_k()
+        marks[r + 1].record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
     if graphed:   # the dominant kernel's durations: the same K steps with events
         with torch.cuda.stream(stream):
             graph_ev.replay()
         torch.cuda.synchronize()
-    wall1 = time.time()
     if world > 1:
         dist.barrier()
-    ms_total = t_begin.elapsed_time(t_end)
+    rep_ms = [marks[r].elapsed_time(marks[r + 1]) for r in range(n_rep)]
+    ms_total = statistics.median(rep_ms)
     lookup_ms = [a.elapsed_time(b) for a, b in ev]
     ms_total = max_over_ranks(ms_total, device)
     code, flags = eg.engram_read_status(step.status, stream)
@@ -531,11 +591,21 @@ def run_native(args):
                 "lookup_ms_mean": lk,
                 "lookup_ms_median": statistics.median(lookup_ms),
             },
-            "gpu_launches": step.launches * K,
-            "launch_mode": ("one CUDA graph of the K steps, replayed once (captured and "
-                            "replayed once untimed before); the dominant kernel timed in a "
-                            "second replay of the same K steps with CUDA events around its "
-                            "launches") if graphed else "eager (events around the dominant kernel)",
+            "gpu_launches": step.launches * K * n_rep,
+            "gpu_launches_per_step": step.launches,
+            "replays": n_rep,
+            "timed_region_s": sum(rep_ms) * 1e-3,
+            "replay_ms": {"min": min(rep_ms), "median": statistics.median(rep_ms),
+                          "max": max(rep_ms)},
+            "launch_mode": ("one CUDA graph of the K steps (captured, then replayed twice "
+                            "untimed); the timed region replays it back to back, each replay of "
+                            "exactly K steps between CUDA events, until the region lasts "
+                            f"{args.min_timed_s:g} s ({n_rep} replays; ms_per_step and value "
+                            "from the median replay); the dominant kernel timed in a further "
+                            "replay of the same K steps with CUDA events around its launches")
+                           if graphed else
+                           f"eager, {n_rep} timed rounds of K steps (median round; events around "
+                           "the dominant kernel)",
             "status_flags": flags,
             "clocks": clk,
         }

@@ -16,10 +16,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_stream_rotation_reads_every_step_from_hbm():
-    # a decode step's 16.8 MB of streams fit in L2: rotate until the buffers exceed it twice
+    # a decode step's 16.8 MB of streams (in and out twice that) and 25.2 MB of rows fit
+    # in L2: rotate input sets until they exceed it twice
     dec = W.by_name("decode_fp8")
     n = bench.stream_rotation(dec)
-    assert n > 1 and n * dec.T * 4 * dec.width * 2 * 2 >= 2 * bench.L2_BYTES
+    assert bench.step_footprint(dec) == 512 * 4 * 4096 * 2 * 2 + 512 * 12 * 4100
+    assert n > 1 and n * bench.step_footprint(dec) >= 2 * bench.L2_BYTES
+    assert (n - 1) * bench.step_footprint(dec) < 2 * bench.L2_BYTES   # no more sets than needed
     for name in ("mid_prefill_fp8", "full_prefill_fp8", "release_layout_fp8"):
         assert bench.stream_rotation(W.by_name(name)) == 1
     assert "rotation" in bench.l2_note(dec) and "no flush" in bench.l2_note(W.by_name("mid_prefill_fp8"))
@@ -76,3 +79,12 @@ def test_reference_arm_prints_one_json_line():
                         "d2h_bytes_per_step": 0}
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+
+
+def test_replays_fill_the_timed_region():
+    # a 33 ms replay of K steps: 31 replays make the first region of >= 1 s
+    assert bench.replays_for(0.033, 1.0) == 31
+    assert bench.replays_for(2.0, 1.0) == 1           # one replay already long enough
+    assert bench.replays_for(1e-9, 1.0) == bench.MAX_REPLAYS
+    assert bench.replays_for(0.0, 1.0) == 1
+    assert bench.replays_for(0.25, 0.0) == 1          # --min-timed-s 0: exactly one replay
