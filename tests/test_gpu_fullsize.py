@@ -5,7 +5,9 @@ tables and streams are generated on the GPU, token ids on the host.  Every
 compressed id and every row id is checked against the oracle; the streams are
 checked on a seeded sample of tokens, for which the oracle gets exactly the
 table rows and stream values the GPU read (copied back from the device: inputs,
-not results)."""
+not results).  A decode step's streams are checked on every slot; a
+prefill's on 4096 sampled tokens (the first, the last and a seeded draw),
+handed to the oracle in batches of 1024."""
 import numpy as np
 import pytest
 
@@ -15,7 +17,8 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-N_SAMPLE = 192
+N_SAMPLE = 4096
+ORACLE_BATCH = 1024
 
 
 @pytest.fixture(scope="module")
@@ -74,6 +77,32 @@ def device_inputs(eg, cfg):
                 tables=eg.Tables(dt, tabs, scales))
 
 
+def check_streams(cfg, d, out, r_all, toks):
+    """The oracle's streams for tokens `toks`, from exactly the table rows and
+    stream values the GPU read (copied back), against the GPU's."""
+    import torch
+    T = cfg.T
+    rr = r_all[toks]                                      # [K, 3H]
+    tabs, scs, remap = [], [], np.empty_like(rr)
+    for n in range(3):
+        cols = slice(n * cfg.H, (n + 1) * cfg.H)
+        live = rr[:, cols] != oracle.DEAD
+        uniq, inv = np.unique(np.where(live, rr[:, cols], 0), return_inverse=True)
+        remap[:, cols] = np.where(live, inv.reshape(rr[:, cols].shape), oracle.DEAD)
+        idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
+        t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
+        tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
+        scs.append(d["tables"].scales[n].index_select(0, idx).cpu().numpy()
+                   if cfg.dtype != W.BF16 else None)
+    sel = torch.from_numpy(np.ascontiguousarray(toks)).cuda()
+    x = d["streams"].view(T, 4, cfg.D)[sel].cpu().numpy().view(np.uint16)
+    y_ref, f3 = oracle.lookup(remap, cfg.H, P.oracle_dtype(cfg), tabs, scs, x,
+                              d["alpha"].cpu().numpy(), cfg.eps)
+    assert f3 == 0
+    y = out.view(T, 4, cfg.D)[sel].cpu().numpy().view(np.uint16)
+    P.compare_streams(y, y_ref, x, what=f"{cfg.name} streams of tokens {toks[0]}..{toks[-1]}")
+
+
 @pytest.mark.parametrize("name", ["mid_prefill_fp8", "decode_fp8", "full_prefill_fp8", "bf16_tables",
                                   "packed_mm_fp8", "full_prefill_fp8_e8m0", "release_layout_fp8"])
 def test_full_size_sampled(eg, name):
@@ -108,27 +137,19 @@ def test_full_size_sampled(eg, name):
     if hist_out is not None:
         assert np.array_equal(hist_out.cpu().numpy(), h_ref)
 
-    # streams on a seeded sample of tokens (first, last, random)
-    g = np.random.default_rng(1000 + cfg.seed)
+    # streams: every slot of a decode step, else a seeded sample of tokens
+    # (first, last, random), in batches the oracle finishes quickly
     T = cfg.T
-    toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(N_SAMPLE, T), replace=False)]))
-    rr = r_ref.reshape(T, -1)[toks]                       # [K, 3H]
-    tabs, scs, remap = [], [], np.empty_like(rr)
-    for n in range(3):
-        cols = slice(n * cfg.H, (n + 1) * cfg.H)
-        live = rr[:, cols] != oracle.DEAD
-        uniq, inv = np.unique(np.where(live, rr[:, cols], 0), return_inverse=True)
-        remap[:, cols] = np.where(live, inv.reshape(rr[:, cols].shape), oracle.DEAD)
-        idx = torch.from_numpy(uniq.astype(np.int64)).cuda()
-        t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
-        tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
-        scs.append(d["tables"].scales[n].index_select(0, idx).cpu().numpy()
-                   if cfg.dtype != W.BF16 else None)
-    x = d["streams"].view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
-    y_ref, f3 = oracle.lookup(remap, cfg.H, P.oracle_dtype(cfg), tabs, scs, x,
-                              d["alpha"].cpu().numpy(), cfg.eps)
-    assert f3 == 0
-    y = out.view(T, 4, cfg.D)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
-    P.compare_streams(y, y_ref, x, what=f"{cfg.name} sampled streams")
+    if cfg.decode:
+        toks = np.arange(T)
+    else:
+        g = np.random.default_rng(1000 + cfg.seed)
+        toks = np.unique(np.concatenate([[0, T - 1], g.choice(np.arange(1, T - 1),
+                                                             size=min(N_SAMPLE - 2, T - 2),
+                                                             replace=False)]))
+    assert len(toks) >= min(N_SAMPLE, T)
+    r_all = r_ref.reshape(T, -1)
+    for b0 in range(0, len(toks), ORACLE_BATCH):
+        check_streams(cfg, d, out, r_all, toks[b0:b0 + ORACLE_BATCH])
     del d, out, rows, eids
     torch.cuda.empty_cache()
