@@ -2,6 +2,13 @@
 // one launch, for sm_103a: compression of the slot's token, its window from the
 // slot's three-id history, the hash into row ids kept in shared memory, and the
 // one-token-a-block bulk lookup body on them.
+//
+// The launch allows programmatic dependent launch: each block first waits for
+// the previous grid on the stream to finish (griddepcontrol.wait, before any
+// memory access, so the result never depends on what that grid wrote), then
+// lets the next grid be scheduled into the room it leaves.  Back to back, a
+// step's blocks are then resident when the previous step ends instead of being
+// launched after it.
 #include <atomic>
 
 #include "bulk_copy.cuh"
@@ -29,6 +36,8 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   __shared__ int s_skip, s_dead;
   const int64_t b = blockIdx.x;
   const int H = p.lk.H, R = 3 * H;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // The slot's streams do not depend on its token: their HBM reads start now,
   // under the dependent loads of the token and its map entry.
   if (threadIdx.x == 32) prefetch_l2(p.lk.x + b * 4 * p.lk.D, (uint32_t)(8 * p.lk.D));
@@ -87,8 +96,17 @@ cudaError_t launch_decode_t(const DecodeParams &p, size_t smem, cudaStream_t str
   static std::atomic<uint64_t> configured{0};
   const cudaError_t e = raise_smem_ceiling(kern, configured);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.lk.T, p.lk.D / 16, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.lk.T);
+  cfg.blockDim = dim3((unsigned)(p.lk.D / 16));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int DT>
@@ -102,6 +120,9 @@ cudaError_t launch_decode_dt(const DecodeParams &p, size_t smem, bool aux, bool 
 }
 
 }  // namespace
+
+// The slot's block is the one-token-a-block lookup's: the same shape limits.
+bool decode_supported(int D, int dtype, int H) { return bulk_supported(D, dtype, H); }
 
 cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream) {
   if (p.lk.T == 0) return cudaSuccess;

@@ -456,6 +456,13 @@ engram_status engram::prepare_lookup(const char *fn, const int32_t *row_ids, boo
 
 int engram::lookup_kernel_choice() { return g_lookup_kernel.load(std::memory_order_relaxed); }
 
+bool engram::take_withheld_launch() {
+  int w = g_withhold.load(std::memory_order_relaxed);
+  while (w > 0 && !g_withhold.compare_exchange_weak(w, w - 1)) {
+  }
+  return w > 0;
+}
+
 extern "C" {
 
 ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_tokens,
@@ -476,10 +483,7 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
   const bool bulk = bulk_family && engram::bulk_supported(D, tb.dtype, n_heads);
   const bool small = bulk_family && !bulk && engram::bulk_small_supported(D, tb.dtype, n_heads);
   if (bulk || small) {
-    int w = g_withhold.load(std::memory_order_relaxed);
-    while (w > 0 && !g_withhold.compare_exchange_weak(w, w - 1)) {
-    }
-    p.withhold = w > 0 ? 1 : 0;
+    p.withhold = engram::take_withheld_launch() ? 1 : 0;
     if (small)
       return launched("engram_lookup_fused launch (bulk, small rows)",
                       engram::launch_lookup_bulk_small(p, tb.dtype, (cudaStream_t)stream));

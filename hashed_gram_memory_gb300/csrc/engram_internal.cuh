@@ -78,7 +78,7 @@ struct LookupParams {
   int32_t H, D;
   int32_t tpt;  // gather kernel: threads per token (16 columns each)
   int32_t tpb;  // gather kernel: tokens per block
-  int32_t withhold; // bulk kernel test hook: withhold one row copy per block
+  int32_t withhold; // test hook: withhold one row copy per block (bulk kernels, decode step)
   int64_t wait_limit_ns;
   float eps, inv_R, inv_D, sqrt_D;
 };
@@ -106,6 +106,7 @@ cudaError_t launch_lookup(const LookupParams &p, int dtype, cudaStream_t stream)
 cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_supported(int D, int dtype, int H);
 size_t bulk_smem_bytes(int D, int dtype, int H);  // one token's rows, scales and barrier
+bool decode_supported(int D, int dtype, int H);  // the fused decode step's shape limits
 cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t stream);
 cudaError_t launch_lookup_bulk_small(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_small_supported(int D, int dtype, int H);
@@ -131,6 +132,9 @@ engram_status prepare_lookup(const char *fn, const int32_t *row_ids, bool need_r
                              float eps, float *gate_out, float *mem_out, int32_t *status,
                              LookupParams &p);
 int lookup_kernel_choice();
+// The test hook of engram_debug_withhold_copies: true (and one launch fewer left)
+// while launches are to withhold a row copy.
+bool take_withheld_launch();
 // engram_forward runs this call as the fused decode launch (no workspace used).
 bool forward_is_decode_step(int32_t batch, int32_t seq, int32_t n_heads,
                             const engram_tables *tables_host);

@@ -139,6 +139,7 @@ engram_status decode_step(const int32_t *token_ids, int32_t batch, const int32_t
   st = engram::prepare_lookup(fn, nullptr, false, batch, n_heads, tables_host, streams_in,
                               streams_out, alpha, eps, nullptr, nullptr, status, p.lk);
   if (st != ENGRAM_OK) return st;
+  p.lk.withhold = engram::take_withheld_launch() ? 1 : 0;
   p.token_ids = token_ids;
   p.tid2eid = tid2eid;
   p.history = history;
@@ -170,7 +171,7 @@ bool forward_is_decode_step(int32_t batch, int32_t seq, int32_t n_heads,
   if (seq != 1 || batch < 1 || !tables_host) return false;
   const int which = lookup_kernel_choice();
   return (which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
-         bulk_supported(tables_host->D, tables_host->dtype, n_heads);
+         decode_supported(tables_host->D, tables_host->dtype, n_heads);
 }
 
 }  // namespace engram
@@ -401,7 +402,7 @@ ENGRAM_API engram_status engram_forward_host(
   const size_t buf = round_up(chunk * tok_bytes);
   const int which = engram::lookup_kernel_choice();
   if (seq == 1 && (which == ENGRAM_LOOKUP_AUTO || which == ENGRAM_LOOKUP_BULK) &&
-      engram::bulk_supported(D, tables_host->dtype, n_heads)) {
+      engram::decode_supported(D, tables_host->dtype, n_heads)) {
     // A decode step: each chunk of slots is one fused launch (compression,
     // window, hash and lookup), as engram_forward runs it; only the ids move
     // in ahead of the streams.

@@ -546,10 +546,10 @@ ENGRAM_API int64_t engram_set_wait_limit_ns(int64_t ns);
 
 /*
  * Test hook for the timeout path: the next `launches` launches of the BULK
- * lookup kernel withhold one row copy in every block (the mbarrier still
- * expects its bytes), so the block's bounded wait runs out, the block skips its
- * token, and the launch reports ENGRAM_FLAG_TIMEOUT.  For tests only; 0 turns
- * it off.
+ * lookup kernels or of the fused decode step (engram_forward with seq = 1)
+ * withhold one row copy in every block (the mbarrier still expects its bytes),
+ * so the block's bounded wait runs out, the block skips its token or slot, and
+ * the launch reports ENGRAM_FLAG_TIMEOUT.  For tests only; 0 turns it off.
  */
 ENGRAM_API void engram_debug_withhold_copies(int32_t launches);
 

@@ -178,6 +178,42 @@ def test_bulk_kernel_bounded_wait_times_out_and_context_survives(eg, shape):
         eg.engram_set_lookup_kernel(prev_k)
 
 
+def test_decode_step_bounded_wait_times_out_and_context_survives(eg):
+    """The fused decode launch with a withheld row copy in every slot: each
+    slot's bounded wait on that row runs out, the launch ends by itself with
+    ENGRAM_FLAG_TIMEOUT and leaves every slot's streams unwritten, and the next
+    decode step on the same context matches the oracle."""
+    import torch
+    cfg = W.by_name("decode_fp8").scaled(B=40, rows=(7001, 7013, 7019))
+    inp = P.host_inputs(cfg)
+    ref = P.oracle_path(inp)
+    dev = P.to_device(inp)
+    prev_l = eg.engram_set_wait_limit_ns(5_000_000)
+    try:
+        eg.engram_debug_withhold_copies(1)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full_like(dev["streams"], 0x5555)
+        eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                          dev["streams"], dev["alpha"], cfg.eps, history=dev["history"],
+                          streams_out=out, status=st)
+        code, flags = eg.engram_read_status(st)
+        assert code == eg.ERR_TIMEOUT and flags & eg.FLAG_TIMEOUT
+        assert bool((out == 0x5555).all()), "a timed-out slot wrote its streams"
+        torch.cuda.synchronize()
+        st.zero_()
+        hist_out = torch.empty_like(dev["history"])
+        again = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                                  dev["streams"], dev["alpha"], cfg.eps, history=dev["history"],
+                                  history_out=hist_out, status=st)
+        assert eg.engram_read_status(st)[1] == 0
+        P.compare_streams(again.cpu().numpy().view(np.uint16), ref["streams"], inp.streams,
+                          what="decode step after a timeout")
+        assert np.array_equal(hist_out.cpu().numpy(), ref["history"])
+    finally:
+        eg.engram_debug_withhold_copies(0)
+        eg.engram_set_wait_limit_ns(prev_l)
+
+
 @pytest.mark.parametrize("pos", [0, 1, 2, 3, 40])
 def test_decode_positions_and_dead_history_match_oracle(eg, pos):
     """Decode steps of packed requests: the start position bounds how far back the

@@ -135,6 +135,27 @@ def test_fused_decode_equals_three_calls(eg, B, dtype, with_history, in_place_hi
         assert torch.equal(h_out, h_sep)
 
 
+@pytest.mark.parametrize("D,H,dtype", [(512, 4, W.FP8), (1024, 4, W.FP8), (2048, 8, W.FP8_E8M0),
+                                       (3072, 2, W.BF16)])
+def test_decode_step_other_widths_match_oracle(eg, D, H, dtype):
+    """One new token a slot at other row widths through the fused decode launch:
+    one warp a slot (D 512), two (D 1024), 8 heads of e8m0-blocked rows (D 2048),
+    BF16 rows of 3072 (six warps): streams and history against the oracle."""
+    import torch
+    cfg, inp, dev, hist = _decode_case(eg, B=129, H=H, D=D, dtype=dtype, rows=(5003, 5009, 5011))
+    ref = P.oracle_path(P.HostInputs(cfg, inp.ids, inp.tid2eid, hist.cpu().numpy(), inp.tables,
+                                     inp.scales, inp.streams, inp.alpha))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h_out = torch.empty_like(hist)
+    y = eg.engram_forward(dev["ids"], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"],
+                          dev["streams"], dev["alpha"], cfg.eps, history=hist, history_out=h_out,
+                          status=st)
+    assert eg.engram_read_status(st)[1] == 0 and ref["flags"] == 0
+    P.compare_streams(y.cpu().numpy().view(np.uint16), ref["streams"], inp.streams,
+                      what=f"decode D={D} H={H} {dtype}")
+    assert np.array_equal(h_out.cpu().numpy(), ref["history"])
+
+
 def test_fused_decode_bad_token_leaves_its_slot_unwritten(eg):
     """A token id outside the vocabulary flags ENGRAM_FLAG_BAD_TOKEN and leaves
     that slot's streams and history unwritten; the other slots are exact."""
