@@ -47,9 +47,9 @@ METRIC = "Engram fused lookup tokens/s and achieved HBM GB/s (% of GB300 peak), 
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lookup_fused_traffic.json")
 # The timed region replays the K steps until it has lasted this long, so that the
-# clock sampler (one sample every 100 ms) sees it; at most MAX_REPLAYS replays.
+# clock sampler (one sample every 100 ms) sees it.
 MIN_TIMED_S = 1.0
-MAX_REPLAYS = 20000
+REPLAYS_PER_ROUND = 8
 
 
 def parse():
@@ -78,15 +78,6 @@ def parse():
     ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
                     help="replay the K timed steps until the timed region lasts this long")
     return ap.parse_args()
-
-
-def replays_for(replay_s: float, min_timed_s: float = MIN_TIMED_S) -> int:
-    """How many back-to-back replays of the K steps make a timed region of at
-    least min_timed_s, given one replay's duration (at least one, at most
-    MAX_REPLAYS)."""
-    if replay_s <= 0:
-        return 1
-    return int(max(1, min(MAX_REPLAYS, -(-min_timed_s // replay_s))))
 
 
 def config_of(name: str, args=None) -> W.EngramConfig:
@@ -275,7 +266,8 @@ class ClockSampler:
 def device_inputs(eg, cfg, rank, device):
     import torch
     tabs, scales = W.tables_device(cfg, device)
-    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16}[cfg.dtype]
+    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16,
+          W.FP8_E8M0_ROWS: eg.TABLE_FP8_E8M0_ROWS}[cfg.dtype]
     hist = W.history(cfg, rank)
     pos, dead = W.packed_layout(cfg, rank) if cfg.packed else (None, None)
     return dict(
@@ -430,6 +422,7 @@ def run_native(args):
     def rot(i):
         k = i % n_rot
         return dict(x=xs_rot[k], out=ys_rot[k], ids=ids_rot[k], hist=hist_rot[k])
+
     # The K timed steps are captured once into a CUDA graph and replayed, so the
     # GPU runs them back to back without waiting on Python between launches.
     # The step throughput comes from a graph of the K steps alone; the dominant
@@ -439,7 +432,6 @@ def run_native(args):
     graphed = not args.eager and graph_timing_supported()
     ev_kw = {"enable_timing": True, "external": True} if graphed else {"enable_timing": True}
     ev = [(torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)) for _ in range(K)]
-    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     graph = graph_ev = None
     if graphed:
         graph = torch.cuda.CUDAGraph()
@@ -464,35 +456,39 @@ def run_native(args):
             for i in range(K):
                 step(ev[i][0], ev[i][1], **rot(i))
 
-    # One untimed replay sizes the timed region: enough replays of the K steps
-    # to last MIN_TIMED_S.
-    t_begin.record(stream)
-    run_k()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    n_rep = replays_for(t_begin.elapsed_time(t_end) * 1e-3, args.min_timed_s)
-    if world > 1:   # every rank replays as often as rank 0
-        n_rep = int(max_over_ranks(float(n_rep), device))
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    # The timed region: replays of the K steps back to back, each between CUDA
+    # events, in rounds of REPLAYS_PER_ROUND; a round ends with a synchronize
+    # (between two replays' events, so no replay's time holds the gap), and
+    # rounds go on until the region has lasted --min-timed-s on the wall clock
+    # (every rank as long as the slowest).
     clocks = ClockSampler(local) if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    marks[0].record(stream)
-    for r in range(n_rep):
-        run_k()
-        marks[r + 1].record(stream)
-    torch.cuda.synchronize()
+    rep_ms = []
+    while True:
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(REPLAYS_PER_ROUND + 1)]
+        marks[0].record(stream)
+        for r in range(REPLAYS_PER_ROUND):
+            run_k()
+            marks[r + 1].record(stream)
+        torch.cuda.synchronize()
+        rep_ms += [marks[r].elapsed_time(marks[r + 1]) for r in range(REPLAYS_PER_ROUND)]
+        more = 1.0 if time.time() - wall0 < args.min_timed_s else 0.0
+        if world > 1:
+            more = max_over_ranks(more, device)
+        if not more:
+            break
     wall1 = time.time()
+    n_rep = len(rep_ms)
     if graphed:   # the dominant kernel's durations: the same K steps with events
         with torch.cuda.stream(stream):
             graph_ev.replay()
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    rep_ms = [marks[r].elapsed_time(marks[r + 1]) for r in range(n_rep)]
     ms_total = statistics.median(rep_ms)
     lookup_ms = [a.elapsed_time(b) for a, b in ev]
     ms_total = max_over_ranks(ms_total, device)
@@ -599,12 +595,13 @@ def run_native(args):
                           "max": max(rep_ms)},
             "launch_mode": ("one CUDA graph of the K steps (captured, then replayed twice "
                             "untimed); the timed region replays it back to back, each replay of "
-                            "exactly K steps between CUDA events, until the region lasts "
-                            f"{args.min_timed_s:g} s ({n_rep} replays; ms_per_step and value "
+                            f"exactly K steps between CUDA events, in rounds of {REPLAYS_PER_ROUND} "
+                            "replays with a synchronize between rounds, until the region has "
+                            f"lasted {args.min_timed_s:g} s ({n_rep} replays; ms_per_step and value "
                             "from the median replay); the dominant kernel timed in a further "
                             "replay of the same K steps with CUDA events around its launches")
                            if graphed else
-                           f"eager, {n_rep} timed rounds of K steps (median round; events around "
+                           f"eager, {n_rep} timed runs of K steps (median run; events around "
                            "the dominant kernel)",
             "status_flags": flags,
             "clocks": clk,
@@ -779,7 +776,12 @@ def oracle_sample(cfg, d, n_tokens):
         remap[:, cols] = np.where(live, inv.reshape(r[:, cols].shape), oracle.DEAD)
         idx = torch.from_numpy(uniq.astype(np.int64)).to(d["tables"].tables[k].device)
         t = d["tables"].tables[k].index_select(0, idx).cpu().numpy()
-        host_tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
+        t = t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8)
+        if cfg.dtype == W.FP8_E8M0_ROWS:   # the oracle takes the bytes and the exponents apart
+            host_tabs.append(np.ascontiguousarray(t[:, :cfg.D]))
+            host_scales.append(np.ascontiguousarray(t[:, cfg.D:cfg.D + cfg.D // 32]))
+            continue
+        host_tabs.append(t)
         host_scales.append(d["tables"].scales[k].index_select(0, idx).cpu().numpy()
                            if cfg.dtype != W.BF16 else None)
     wkv = d["wkv"].cpu().numpy().view(np.uint16) if cfg.hidden else None
@@ -790,7 +792,8 @@ def oracle_sample(cfg, d, n_tokens):
 
 def oracle_dtype(cfg):
     import oracle
-    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.BF16: oracle.BF16}[cfg.dtype]
+    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.FP8_E8M0_ROWS: oracle.FP8_E8M0,
+            W.BF16: oracle.BF16}[cfg.dtype]
 
 
 def time_oracle(cfg, s, repeats=1):
@@ -872,7 +875,7 @@ def reference_sample(cfg, n):
         if cfg.dtype == W.FP8:
             tabs.append(W._to_e4m3_bytes(x))
             scs.append(g.uniform(cfg.scale_lo, cfg.scale_hi, len(uniq)).astype(np.float32))
-        elif cfg.dtype == W.FP8_E8M0:
+        elif cfg.dtype in (W.FP8_E8M0, W.FP8_E8M0_ROWS):   # the oracle reads both alike
             tabs.append(W._to_e4m3_bytes(x))
             scs.append(g.integers(cfg.e8m0_lo, cfg.e8m0_hi + 1, size=(len(uniq), cfg.D // 32))
                        .astype(np.uint8))

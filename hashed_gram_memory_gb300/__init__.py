@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libengram.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OUT_OF_RANGE, ERR_TIMEOUT = range(6)
 FLAG_BAD_TOKEN, FLAG_BAD_EID, FLAG_BAD_ROW, FLAG_TIMEOUT = 1, 2, 4, 8
-TABLE_FP8_E4M3FN, TABLE_BF16, TABLE_FP8_E8M0 = 0, 1, 2
+TABLE_FP8_E4M3FN, TABLE_BF16, TABLE_FP8_E8M0, TABLE_FP8_E8M0_ROWS = 0, 1, 2, 3
 EID_DEAD = ROW_DEAD = -1
 LOOKUP_AUTO, LOOKUP_GATHER, LOOKUP_BULK = 0, 1, 2
 PROJECTION_AUTO, PROJECTION_SINGLE, PROJECTION_PAIR = 0, 1, 2
@@ -141,6 +141,8 @@ def _load():
     L.engram_wkv_project.restype = i32
     L.engram_gate_add.argtypes = [vp, vp, i64, i32, vp, vp, vp, C.c_float, vp, vp]
     L.engram_gate_add.restype = i32
+    L.engram_pack_e8m0_rows.argtypes = [vp, vp, i64, i32, vp, vp]
+    L.engram_pack_e8m0_rows.restype = i32
     return L
 
 
@@ -177,11 +179,19 @@ def _need(t, dtypes, name, contiguous=True):
         raise EngramError(ERR_INVALID_ARG, f"{name} must be contiguous")
 
 
+def e8m0_row_bytes(D: int) -> int:
+    """Bytes of one row of a TABLE_FP8_E8M0_ROWS table of width D (the row, its
+    D/32 exponents, zeros up to a multiple of 16)."""
+    return (D + D // 32 + 15) // 16 * 16
+
+
 @dataclasses.dataclass
 class Tables:
     """The three device tables (orders 2, 3, 4) and their scales: fp32 [rows] for
     TABLE_FP8_E4M3FN, uint8 e8m0 exponents [rows, D/32] for TABLE_FP8_E8M0, none
-    for TABLE_BF16."""
+    for TABLE_BF16.  TABLE_FP8_E8M0_ROWS tables are uint8 [rows,
+    e8m0_row_bytes(D)] (engram_pack_e8m0_rows) with no scales; their D is the
+    widest multiple of 32 whose packed row fills the table's row."""
 
     dtype: int
     tables: list
@@ -189,7 +199,15 @@ class Tables:
 
     @property
     def D(self) -> int:
-        return int(self.tables[0].shape[1])
+        width = int(self.tables[0].shape[1])
+        if self.dtype != TABLE_FP8_E8M0_ROWS:
+            return width
+        D = width * 32 // 33 // 32 * 32
+        while D > 0 and e8m0_row_bytes(D) > width:
+            D -= 32
+        if D <= 0 or e8m0_row_bytes(D) != width:
+            raise EngramError(ERR_INVALID_ARG, f"{width} bytes is no packed e8m0 row width")
+        return D
 
     @property
     def rows(self):
@@ -205,6 +223,24 @@ class Tables:
             sc = self.scales[n] if self.scales else None
             s.scale[n] = sc.data_ptr() if sc is not None else None
         return s
+
+
+def engram_pack_e8m0_rows(table, exps, packed=None, stream=None):
+    """A TABLE_FP8_E8M0_ROWS table from a TABLE_FP8_E8M0 one: table uint8 [rows, D],
+    exps uint8 [rows, D/32] -> uint8 [rows, e8m0_row_bytes(D)] (each row, then its
+    exponents, then zeros)."""
+    import torch
+    _need(table, (torch.uint8,), "table")
+    _need(exps, (torch.uint8,), "exps")
+    rows, D = table.shape
+    if tuple(exps.shape) != (rows, D // 32):
+        raise EngramError(ERR_INVALID_ARG, "exps must be [rows, D/32]")
+    if packed is None:
+        packed = torch.empty((rows, e8m0_row_bytes(D)), dtype=torch.uint8, device=table.device)
+    _need(packed, (torch.uint8,), "packed")
+    _check(lib.engram_pack_e8m0_rows(_ptr(table), _ptr(exps), rows, D, _ptr(packed),
+                                     _stream(stream)), "engram_pack_e8m0_rows")
+    return packed
 
 
 def engram_compress(token_ids, tid2eid, n_eids: int, eids_out=None, status=None, stream=None,

@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libengram.so")
 
 SOURCES = ["engram_api.cu", "compress_hash.cu", "lookup_fused.cu", "lookup_bulk.cu",
-           "decode_step.cu", "forward.cu", "forward_static.cu", "wkv_gemm.cu", "connection.cu"]
+           "decode_step.cu", "forward.cu", "forward_static.cu", "wkv_gemm.cu", "connection.cu",
+           "table_pack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

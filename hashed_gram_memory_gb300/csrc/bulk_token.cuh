@@ -23,11 +23,12 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
                                            const int64_t t) {
   constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;                // FP8 bytes
   constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
+  constexpr bool kRows = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS;  // the exponents after each row
   constexpr int kElt = kFp8 ? 1 : 2;
   extern __shared__ __align__(128) uint8_t sm[];
 
   const int H = p.H, R = 3 * H, D = p.D;
-  const uint32_t row_bytes = (uint32_t)D * kElt;
+  const uint32_t row_bytes = table_row_bytes(DT, D);             // a row (+ its exponents)
   const uint32_t exp_bytes = kE8 ? (uint32_t)D / 32 : 0;         // a row's block exponents
   uint8_t *s_rows = sm;                                          // [R][row_bytes]
   uint8_t *s_exps = s_rows + (size_t)R * row_bytes;              // [R][exp_bytes]
@@ -101,7 +102,7 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
   // the 8-head prefill; the same order for the e8m0 exponents measured 0.921 ->
   // 0.914, so they keep theirs).
   float sc = 0.f;
-  if (kFp8 && !kE8 && tid < R) {
+  if (kFp8 && !kE8 && !kRows && tid < R) {
     const int ni = (tid >= H) + (tid >= 2 * H);
     sc = __ldg(static_cast<const float *>(p.scale[ni]) + ids[tid]);
     if (!EARLY) s_scale[tid] = sc;
@@ -115,7 +116,7 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
       xs[s][1] = __ldcs(reinterpret_cast<const uint4 *>(xrow + (int64_t)s * D + 8));
     }
   }
-  if (kFp8 && !kE8) {
+  if (kFp8 && !kE8 && !kRows) {
     if (EARLY && tid < R) s_scale[tid] = sc;
     for (int r = tid + blockDim.x; r < R; r += blockDim.x) {
       const int ni = (r >= H) + (r >= 2 * H);
@@ -142,7 +143,9 @@ __device__ __forceinline__ void bulk_token(const LookupParams &p, const int32_t 
   for (int r = 0; r < R; ++r) {
     const uint8_t *row = src + (size_t)r * row_bytes;
     if (kFp8) {
-      const float scale = kE8 ? e8m0_to_float(s_exps[(size_t)r * exp_bytes + (col0 >> 5)]) : s_scale[r];
+      const float scale = kRows ? e8m0_to_float(row[(D - col0) + (col0 >> 5)])
+                          : kE8 ? e8m0_to_float(s_exps[(size_t)r * exp_bytes + (col0 >> 5)])
+                                : s_scale[r];
       acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), scale);
     } else {
       acc_bf16(acc, *reinterpret_cast<const uint4 *>(row));

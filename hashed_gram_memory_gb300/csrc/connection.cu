@@ -3,7 +3,8 @@
 // (wkv_gemm.cu), then the gate and the add into the four streams.
 //
 //   concat_rows_kernel : one token per block; dequantises its 3H rows (FP8 with
-//                        e8m0 blocks, or BF16) into E[t] = [row_0 | ... | row_3H-1]
+//                        e8m0 blocks, the exponents apart or after each row, or
+//                        BF16) into E[t] = [row_0 | ... | row_3H-1]
 //                        as bf16, 16-byte stores; records the token's state
 //                        (live, dead, bad) for the last kernel.
 //   wkv_gemm_kernel    : k = E wkv^T, fp32.
@@ -34,6 +35,7 @@ struct ConcatParams {
 template <int DT>
 __global__ void __launch_bounds__(256) concat_rows_kernel(const __grid_constant__ ConcatParams p) {
   constexpr bool kBf16 = DT == ENGRAM_TABLE_BF16;
+  constexpr bool kRows = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS;  // the exponents after each row
   const int64_t t = blockIdx.x;
   const int H = p.H, R = 3 * H, d = p.d;
   const int64_t K = (int64_t)R * d;
@@ -75,9 +77,11 @@ __global__ void __launch_bounds__(256) concat_rows_kernel(const __grid_constant_
       lo = __ldg(src);
       hi = __ldg(src + 1);
     } else {
-      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(p.table[ni] + row * d + col));
+      const uint8_t *rbase = p.table[ni] + row * (int64_t)table_row_bytes(DT, d);
+      const uint4 b = __ldg(reinterpret_cast<const uint4 *>(rbase + col));
       const float s = e8m0_to_float(
-          __ldg(static_cast<const uint8_t *>(p.scale[ni]) + row * (d >> 5) + (col >> 5)));
+          kRows ? __ldg(rbase + d + (col >> 5))
+                : __ldg(static_cast<const uint8_t *>(p.scale[ni]) + row * (d >> 5) + (col >> 5)));
       float f[16];
       const uint32_t w[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -200,6 +204,8 @@ cudaError_t launch_concat_rows(const int32_t *row_ids, int64_t T, int H, const e
   cp.d = tb.D;
   if (tb.dtype == ENGRAM_TABLE_BF16)
     concat_rows_kernel<ENGRAM_TABLE_BF16><<<(unsigned)T, 256, 0, stream>>>(cp);
+  else if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
+    concat_rows_kernel<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS><<<(unsigned)T, 256, 0, stream>>>(cp);
   else
     concat_rows_kernel<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32><<<(unsigned)T, 256, 0, stream>>>(cp);
   return cudaGetLastError();

@@ -133,6 +133,8 @@ cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t st
     return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
     return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32>(p, smem, aux, early, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
+    return launch_decode_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS>(p, smem, aux, early, stream);
   return launch_decode_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 

@@ -10,6 +10,7 @@
 #include <atomic>
 
 #include "engram_internal.cuh"
+#include "lookup_common.cuh"
 
 namespace {
 
@@ -383,17 +384,18 @@ engram_status engram::prepare_lookup(const char *fn, const int32_t *row_ids, boo
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
   if (!tables_host) return fail(ENGRAM_ERR_INVALID_ARG, "%s: tables is NULL", fn);
   const engram_tables &tb = *tables_host;
-  if (tb.dtype != ENGRAM_TABLE_FP8_E4M3FN && tb.dtype != ENGRAM_TABLE_BF16 &&
-      tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+  const bool e8m0 = tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 ||
+                    tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS;
+  if (tb.dtype != ENGRAM_TABLE_FP8_E4M3FN && tb.dtype != ENGRAM_TABLE_BF16 && !e8m0)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: unknown table dtype %d", fn, tb.dtype);
   if (tb.D < 16 || tb.D % 16 != 0)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: D = %d must be a positive multiple of 16", fn, tb.D);
-  if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && tb.D % 32 != 0)
+  if (e8m0 && tb.D % 32 != 0)
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: E8M0 (1, 32) blocks need D %% 32 == 0", fn);
   if (tb.D > ENGRAM_MAX_D)
     return fail(ENGRAM_ERR_UNSUPPORTED, "%s: D = %d exceeds %d", fn, tb.D, ENGRAM_MAX_D);
   const int D = tb.D;
-  const size_t elt = tb.dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
+  const size_t table_row = engram::table_row_bytes(tb.dtype, D);
   for (int n = 0; n < 3; ++n) {
     if (tb.rows[n] < 1 || tb.rows[n] > INT32_MAX)
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: rows[%d] must be in [1, 2^31-1]", fn, n);
@@ -425,7 +427,7 @@ engram_status engram::prepare_lookup(const char *fn, const int32_t *row_ids, boo
         (gate_out && overlap(gate_out, (size_t)n_tokens * 4, streams_out, sbytes)))
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: output buffers overlap", fn);
     for (int n = 0; n < 3; ++n)
-      if (overlap(streams_out, sbytes, tb.table[n], (size_t)tb.rows[n] * D * elt))
+      if (overlap(streams_out, sbytes, tb.table[n], (size_t)tb.rows[n] * table_row))
         return fail(ENGRAM_ERR_INVALID_ARG, "%s: streams_out overlaps table[%d]", fn, n);
   }
   if (n_tokens == 0) return ok();
@@ -509,7 +511,8 @@ static engram_status check_connection_tables(const char *fn, int32_t n_heads,
     return fail(ENGRAM_ERR_INVALID_ARG, "%s: n_heads must be in [1, %d]", fn, ENGRAM_MAX_HEADS);
   if (!tables_host) return fail(ENGRAM_ERR_INVALID_ARG, "%s: tables is NULL", fn);
   const engram_tables &tb = *tables_host;
-  if (tb.dtype != ENGRAM_TABLE_BF16 && tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
+  if (tb.dtype != ENGRAM_TABLE_BF16 && tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 &&
+      tb.dtype != ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
     return fail(ENGRAM_ERR_UNSUPPORTED,
                 "%s: the projection takes BF16 or FP8 + e8m0 tables (exact in bf16)", fn);
   if (tb.D < 32 || tb.D % 32 != 0 || tb.D > 65536)
@@ -517,7 +520,7 @@ static engram_status check_connection_tables(const char *fn, int32_t n_heads,
   for (int n = 0; n < 3; ++n) {
     if (tb.rows[n] < 1 || tb.rows[n] > INT32_MAX || !tb.table[n] || !aligned(tb.table[n], 16))
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: table[%d] bad (rows, NULL or alignment)", fn, n);
-    if (tb.dtype != ENGRAM_TABLE_BF16 && !tb.scale[n])
+    if (tb.dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && !tb.scale[n])
       return fail(ENGRAM_ERR_INVALID_ARG, "%s: scale[%d] is NULL", fn, n);
   }
   return ENGRAM_OK;
@@ -648,6 +651,29 @@ ENGRAM_API engram_status engram_connection(const int32_t *row_ids, int64_t n_tok
                                             streams_in, streams_out, alpha, eps, e, k, state,
                                             gate_out, g_wait_limit_ns.load(std::memory_order_relaxed),
                                             status, (cudaStream_t)stream));
+}
+
+ENGRAM_API engram_status engram_pack_e8m0_rows(const uint8_t *table, const uint8_t *exps,
+                                               int64_t rows, int32_t D, uint8_t *packed,
+                                               void *stream) {
+  ENGRAM_NVTX_RANGE("engram_pack_e8m0_rows");
+  const char *fn = "engram_pack_e8m0_rows";
+  if (rows < 0 || D < 32 || D % 32 != 0 || D > ENGRAM_MAX_D)
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: rows >= 0 and D a multiple of 32 in [32, %d]", fn,
+                ENGRAM_MAX_D);
+  if (rows == 0) return ok();
+  if (!table || !exps || !packed || !aligned(table, 16) || !aligned(packed, 16))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: NULL pointer, or table / packed not 16-byte aligned",
+                fn);
+  const size_t nt = (size_t)rows * D, ne = (size_t)rows * (D / 32);
+  const size_t np = (size_t)rows * (size_t)ENGRAM_E8M0_ROW_BYTES(D);
+  if (overlap(packed, np, table, nt) || overlap(packed, np, exps, ne))
+    return fail(ENGRAM_ERR_INVALID_ARG, "%s: packed overlaps an input", fn);
+  engram_status st = check_device();
+  if (st != ENGRAM_OK) return st;
+  return launched("engram_pack_e8m0_rows launch",
+                  engram::launch_pack_e8m0_rows(table, exps, rows, D, packed,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 ENGRAM_API int32_t engram_set_lookup_kernel(int32_t which) {

@@ -111,6 +111,9 @@ cudaError_t launch_decode_step(const DecodeParams &p, int dtype, cudaStream_t st
 cudaError_t launch_lookup_bulk_small(const LookupParams &p, int dtype, cudaStream_t stream);
 bool bulk_small_supported(int D, int dtype, int H);
 
+cudaError_t launch_pack_e8m0_rows(const uint8_t *table, const uint8_t *exps, int64_t rows, int D,
+                                  uint8_t *packed, cudaStream_t stream);
+
 bool wkv_gemm_supported(int N, int K);
 int set_projection_kernel(int which);  // returns the previous choice
 cudaError_t launch_wkv_gemm(const uint16_t *e, const uint16_t *wkv, float *k_out, int T, int N, int K,

@@ -72,11 +72,12 @@ __global__ void __launch_bounds__(256, 2)
     lookup_bulk_small_kernel(const __grid_constant__ LookupParams p) {
   constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;
   constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;
+  constexpr bool kRows = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS;  // the exponents after each row
   constexpr int kElt = kFp8 ? 1 : 2;
   extern __shared__ __align__(128) uint8_t sm[];
 
   const int H = p.H, R = 3 * H, D = p.D, tpt = p.tpt, tpb = p.tpb;
-  const uint32_t row_bytes = (uint32_t)D * kElt;
+  const uint32_t row_bytes = table_row_bytes(DT, D);
   const uint32_t exp_bytes = kE8 ? (uint32_t)D / 32 : 0;
   const size_t tok_bytes = (size_t)R * row_bytes;
   uint8_t *s_rows = sm;                                            // [tpb][R][row_bytes]
@@ -145,10 +146,11 @@ __global__ void __launch_bounds__(256, 2)
     else
       bulk_g2s(dst + (size_t)r * row_bytes, p.table[ni] + id * row_bytes, row_bytes, bar);
     if (kE8) return load_exps(static_cast<const uint8_t *>(p.scale[ni]) + id * exp_bytes, exp_bytes);
-    if (kFp8) return __float_as_uint(__ldg(static_cast<const float *>(p.scale[ni]) + id));
+    if (kFp8 && !kRows) return __float_as_uint(__ldg(static_cast<const float *>(p.scale[ni]) + id));
     return 0;
   };
   auto store_row = [&](int r, uint64_t w) {
+    if (kRows) return;
     if (kE8)
       store_exps(s_exps + ((size_t)tl * R + r) * exp_bytes, w, exp_bytes);
     else if (kFp8)
@@ -193,8 +195,10 @@ __global__ void __launch_bounds__(256, 2)
     for (int r = 0; r < R; ++r) {
       const uint8_t *row = src + (size_t)r * row_bytes;
       if (kFp8) {
-        const float scale = kE8 ? e8m0_to_float(s_exps[((size_t)tl * R + r) * exp_bytes + (col0 >> 5)])
-                                : s_scale[(size_t)tl * R + r];
+        const float scale =
+            kRows ? e8m0_to_float(row[(D - col0) + (col0 >> 5)])
+            : kE8 ? e8m0_to_float(s_exps[((size_t)tl * R + r) * exp_bytes + (col0 >> 5)])
+                  : s_scale[(size_t)tl * R + r];
         acc_fp8(acc, *reinterpret_cast<const uint4 *>(row), scale);
       } else {
         acc_bf16(acc, *reinterpret_cast<const uint4 *>(row));
@@ -269,10 +273,10 @@ cudaError_t launch_small_t(const LookupParams &p, size_t smem, cudaStream_t stre
 
 // Shared memory of the small-row kernel for tpb tokens a block.
 size_t small_smem_bytes(int D, int dtype, int H, int tpb) {
-  const size_t elt = dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
   const size_t rows = (size_t)tpb * 3 * H;
   const size_t exps = dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 ? rows * (D / 32) : 0;
-  return rows * D * elt + ((exps + 15) & ~(size_t)15) + ((rows + 1) & ~(size_t)1) * 4 + 8;
+  return rows * table_row_bytes(dtype, D) + ((exps + 15) & ~(size_t)15) +
+         ((rows + 1) & ~(size_t)1) * 4 + 8;
 }
 
 // Tokens per block, a whole number of warps.  Measured on the released shape
@@ -298,7 +302,9 @@ int small_tokens_per_block(int D, int dtype, int H) {
 // the 227 KB a block may use.
 bool bulk_small_supported(int D, int dtype, int H) {
   if (D < 16 || D >= 512 || ((D / 16) & (D / 16 - 1)) != 0 || D % 16 != 0) return false;
-  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 && D % 32 != 0) return false;
+  if ((dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 || dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS) &&
+      D % 32 != 0)
+    return false;
   return small_smem_bytes(D, dtype, H, small_tokens_per_block(D, dtype, H)) <= 227 * 1024;
 }
 
@@ -315,14 +321,16 @@ cudaError_t launch_lookup_bulk_small(const LookupParams &p_in, int dtype, cudaSt
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
     return aux ? launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, true>(p, smem, stream)
                : launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, false>(p, smem, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
+    return aux ? launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS, true>(p, smem, stream)
+               : launch_small_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS, false>(p, smem, stream);
   return aux ? launch_small_t<ENGRAM_TABLE_BF16, true>(p, smem, stream)
              : launch_small_t<ENGRAM_TABLE_BF16, false>(p, smem, stream);
 }
 
 size_t bulk_smem_bytes(int D, int dtype, int H) {
-  const size_t elt = dtype == ENGRAM_TABLE_BF16 ? 2 : 1;
   const size_t exps = dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 ? (size_t)3 * H * (D / 32) : 0;
-  return (size_t)3 * H * D * elt + exps + 8 + kMaxRows * 4 + 24 * 4;
+  return (size_t)3 * H * table_row_bytes(dtype, D) + exps + 8 + kMaxRows * 4 + 24 * 4;
 }
 
 // D a multiple of 512 (whole warps of 16-column threads, at most 256 threads) and
@@ -343,6 +351,8 @@ cudaError_t launch_lookup_bulk(const LookupParams &p, int dtype, cudaStream_t st
     return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN>(p, smem, aux, early, stream);
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
     return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32>(p, smem, aux, early, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
+    return launch_bulk_dt<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS>(p, smem, aux, early, stream);
   return launch_bulk_dt<ENGRAM_TABLE_BF16>(p, smem, aux, early, stream);
 }
 

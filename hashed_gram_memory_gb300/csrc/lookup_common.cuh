@@ -7,7 +7,17 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include "engram.h"
+
 namespace engram {
+
+// Bytes from one table row to the next: D (FP8), 2D (BF16), and D + D/32
+// padded to 16 for FP8 rows carrying their e8m0 exponents after their bytes.
+__host__ __device__ __forceinline__ uint32_t table_row_bytes(int dtype, int D) {
+  if (dtype == ENGRAM_TABLE_BF16) return 2u * (uint32_t)D;
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS) return (uint32_t)ENGRAM_E8M0_ROW_BYTES(D);
+  return (uint32_t)D;
+}
 
 // OCP E8M0 exponent -> fp32: 2^(e-127) (e = 0 is the fp32 subnormal 2^-127), 0xFF NaN.
 __device__ __forceinline__ float e8m0_to_float(uint32_t e) {

@@ -31,6 +31,7 @@ template <int DT, bool AUX>
 __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ LookupParams p) {
   constexpr bool kFp8 = DT != ENGRAM_TABLE_BF16;           // FP8 bytes (row or block scales)
   constexpr bool kE8 = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;  // one exponent per 32 columns
+  constexpr bool kRows = DT == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS;  // the exponents after each row
   constexpr int kElt = kFp8 ? 1 : 2;         // bytes per table element
   constexpr int kVecPerRow = kFp8 ? 1 : 2;   // 16-byte loads per row per thread
   constexpr int kBatch = kFp8 ? 8 : 4;       // rows in flight per thread
@@ -99,10 +100,13 @@ __global__ void __launch_bounds__(256, 2) lookup_kernel(const __grid_constant__ 
         if (r < R) {
           const int ni = (r >= H) + (r >= 2 * H);
           const int64_t row = ids[r];
-          const uint8_t *base = p.table[ni] + (row * p.D + col0) * kElt;
+          const uint8_t *rbase = p.table[ni] + row * (int64_t)table_row_bytes(DT, p.D);
+          const uint8_t *base = rbase + col0 * kElt;
           v[k][0] = ld_row16(base);
           if (!kFp8) v[k][1] = ld_row16(base + 16);
-          if (kE8)
+          if (kRows)
+            sc[k] = e8m0_to_float(__ldg(rbase + p.D + (col0 >> 5)));
+          else if (kE8)
             sc[k] = e8m0_to_float(__ldg(static_cast<const uint8_t *>(p.scale[ni]) +
                                         row * (p.D >> 5) + (col0 >> 5)));
           else if (kFp8)
@@ -222,6 +226,9 @@ cudaError_t launch_lookup(const LookupParams &p_in, int dtype, cudaStream_t stre
   if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32)
     return aux ? launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, true>(p, threads, smem, stream)
                : launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32, false>(p, threads, smem, stream);
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS)
+    return aux ? launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS, true>(p, threads, smem, stream)
+               : launch_t<ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS, false>(p, threads, smem, stream);
   return aux ? launch_t<ENGRAM_TABLE_BF16, true>(p, threads, smem, stream)
              : launch_t<ENGRAM_TABLE_BF16, false>(p, threads, smem, stream);
 }

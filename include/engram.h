@@ -78,6 +78,10 @@ typedef int32_t engram_status;
 #define ENGRAM_TABLE_FP8_E4M3FN 0
 #define ENGRAM_TABLE_BF16 1
 #define ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 2
+#define ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS 3
+
+/* Bytes of one row of an ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS table of width D. */
+#define ENGRAM_E8M0_ROW_BYTES(D) ((((int64_t)(D) + (int64_t)(D) / 32) + 15) / 16 * 16)
 
 /*
  * Dead positions (image spans: vLLM page, DeepseekV4Model.forward, they break
@@ -102,6 +106,14 @@ typedef int32_t engram_status;
  *    2^(e-127), 0xFF NaN), 16-byte aligned; D % 32 == 0 (VeOmni PR page: the
  *    release blocks its tables (1, 32)).  The products are exact powers of two
  *    times the FP8 value, within the fp32 range.
+ *  - ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS: the values of the previous format with
+ *    each row's exponents stored right after its bytes: row r of table[n] is
+ *    ENGRAM_E8M0_ROW_BYTES(D) bytes, its D e4m3fn bytes, its D/32 e8m0
+ *    exponents, then zero padding to a multiple of 16 bytes; scale[n] unused
+ *    (may be NULL); D % 32 == 0.  Not on the pages: a storage layout of this
+ *    library, made by engram_pack_e8m0_rows, in which a lookup reads a row
+ *    and its exponents as one contiguous run.  Every call gives the same
+ *    results for it as for ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32.
  *  - ENGRAM_TABLE_BF16: two bytes per element; scale[n] ignored.
  * 1 <= rows[n] <= 2^31 - 1.  The struct itself is read on the host during the
  * call only.
@@ -489,6 +501,22 @@ ENGRAM_API engram_status engram_forward_static(
     const engram_tables *tables_host, const engram_layout *layout_host,
     const uint16_t *streams_in, uint16_t *streams_out, const float *alpha, float eps,
     int32_t *status, void *stream);
+
+/*
+ * engram_pack_e8m0_rows -- builds an ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS table
+ * from an ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 one: packed row r = table row r (D
+ * bytes), then exps row r (D/32 bytes), then zeros up to
+ * ENGRAM_E8M0_ROW_BYTES(D).
+ *   table  uint8 [rows, D] (device, 16-byte aligned);
+ *   exps   uint8 [rows, D/32] (device);
+ *   packed uint8 [rows, ENGRAM_E8M0_ROW_BYTES(D)] (device, 16-byte aligned,
+ *          caller-allocated; must not overlap the inputs).
+ * D % 32 == 0, 32 <= D <= ENGRAM_MAX_D, rows >= 0.  Asynchronous on `stream`;
+ * argument errors return before any launch.
+ */
+ENGRAM_API engram_status engram_pack_e8m0_rows(const uint8_t *table, const uint8_t *exps,
+                                               int64_t rows, int32_t D, uint8_t *packed,
+                                               void *stream);
 
 /*
  * engram_read_status -- waits for `stream`, copies the device status word into

@@ -51,7 +51,21 @@ def layer_primes(cfg: W.EngramConfig):
 
 
 def oracle_dtype(cfg: W.EngramConfig) -> int:
-    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.BF16: oracle.BF16}[cfg.dtype]
+    """The oracle's table type: rows carrying their exponents are read, like the
+    separate layout, as bytes plus e8m0 blocks (oracle_tables splits them)."""
+    return {W.FP8: oracle.FP8, W.FP8_E8M0: oracle.FP8_E8M0, W.FP8_E8M0_ROWS: oracle.FP8_E8M0,
+            W.BF16: oracle.BF16}[cfg.dtype]
+
+
+def oracle_tables(cfg: W.EngramConfig, tables, scales):
+    """The tables and scales as the oracle takes them: a table whose rows carry
+    their exponents is split into its bytes [rows, D] and exponents [rows, D/32]
+    (slices of each row, no arithmetic)."""
+    if cfg.dtype != W.FP8_E8M0_ROWS:
+        return tables, scales
+    D = cfg.D
+    return ([np.ascontiguousarray(t[:, :D]) for t in tables],
+            [np.ascontiguousarray(t[:, D:D + D // 32]) for t in tables])
 
 
 def oracle_path(inp: HostInputs):
@@ -66,9 +80,10 @@ def oracle_path(inp: HostInputs):
     else:
         rows, hist, f2 = oracle.hash_ids(eids, cfg.H, cfg.rows, history=inp.history,
                                          want_history=True, positions=inp.positions)
-    y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H, oracle_dtype(cfg), inp.tables,
-                                inp.scales, inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha,
-                                cfg.eps, aux=True)
+    tabs, scs = oracle_tables(cfg, inp.tables, inp.scales)
+    y, g, m, f3 = oracle.lookup(rows.reshape(cfg.T, -1), cfg.H, oracle_dtype(cfg), tabs, scs,
+                                inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha, cfg.eps,
+                                aux=True)
     return dict(eids=eids, rows=rows, history=hist, streams=y.reshape(inp.streams.shape), gate=g,
                 mem=m, flags=f1 | f2 | f3)
 
@@ -91,6 +106,9 @@ def to_device(inp: HostInputs, device="cuda"):
         scs = [torch.from_numpy(s).to(device) for s in inp.scales]
         dt = eg.TABLE_FP8_E4M3FN if cfg.dtype == W.FP8 else eg.TABLE_FP8_E8M0
         dev["tables"] = eg.Tables(dt, tabs, scs)
+    elif cfg.dtype == W.FP8_E8M0_ROWS:
+        tabs = [torch.from_numpy(t).to(device) for t in inp.tables]
+        dev["tables"] = eg.Tables(eg.TABLE_FP8_E8M0_ROWS, tabs, None)
     else:
         tabs = [torch.from_numpy(t.view(np.int16)).to(device) for t in inp.tables]
         dev["tables"] = eg.Tables(eg.TABLE_BF16, tabs, None)

@@ -79,12 +79,3 @@ def test_reference_arm_prints_one_json_line():
                         "d2h_bytes_per_step": 0}
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
-
-
-def test_replays_fill_the_timed_region():
-    # a 33 ms replay of K steps: 31 replays make the first region of >= 1 s
-    assert bench.replays_for(0.033, 1.0) == 31
-    assert bench.replays_for(2.0, 1.0) == 1           # one replay already long enough
-    assert bench.replays_for(1e-9, 1.0) == bench.MAX_REPLAYS
-    assert bench.replays_for(0.0, 1.0) == 1
-    assert bench.replays_for(0.25, 0.0) == 1          # --min-timed-s 0: exactly one replay

@@ -49,6 +49,9 @@ SMALL = {
     # 16,684 tokens: 131 M tiles, about one tile per CTA at the end of the walk
     "many_tiles": BASE.scaled(B=1, S=16384 + 300, H=2, D=64, rows=(1009, 1013, 1019),
                            hash_vocab=0, dtype=W.BF16, hidden=256),
+    # the released row shape with each row's exponents stored after it (272-byte rows)
+    "rows_h8_d256": BASE.scaled(B=1, S=200, H=8, D=256, rows=(3001, 3011, 3019), hash_vocab=0,
+                                hidden=1024, dtype=W.FP8_E8M0_ROWS),
     # packed samples with image spans: dead tokens pass through
     "packed_dead": BASE.scaled(B=2, S=150, H=2, D=128, rows=(1009, 1013, 1019), hash_vocab=0,
                                hidden=256, packed=True, mean_sample_len=64, image_span=16,
@@ -185,7 +188,8 @@ def oracle_rows(cfg, inp):
 
 def oracle_connection(cfg, inp, rows, wkv_bits):
     x = inp.streams.reshape(cfg.T, 4, cfg.hidden)
-    y, g, k, flags = oracle.connection(rows, cfg.H, P.oracle_dtype(cfg), inp.tables, inp.scales,
+    tabs, scs = P.oracle_tables(cfg, inp.tables, inp.scales)
+    y, g, k, flags = oracle.connection(rows, cfg.H, P.oracle_dtype(cfg), tabs, scs,
                                        wkv_bits, x, inp.alpha, cfg.eps, rows=cfg.rows, fill=FILL)
     return y, g, k, flags
 
@@ -205,7 +209,7 @@ def test_connection_parity(eg, name):
     dead = (rows == oracle.DEAD).all(axis=1)
     live = ~dead
     assert live.any()
-    kb, S = k_bound(cfg, wkv, abs_rows(cfg, inp.tables, inp.scales, rows))
+    kb, S = k_bound(cfg, wkv, abs_rows(cfg, *P.oracle_tables(cfg, inp.tables, inp.scales), rows))
     compare_connection(cfg, res, (y_ref, g_ref, k_ref), x, inp.alpha, kb, S, live)
     if dead.any():   # copied through, g = 0, k = 0
         assert np.array_equal(res["streams"][dead], x[dead])

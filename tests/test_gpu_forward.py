@@ -105,6 +105,7 @@ def _decode_case(eg, B=257, H=4, D=4096, rows=(7001, 7013, 7019), with_history=T
 @pytest.mark.parametrize("B,dtype,with_history,in_place_history", [
     (257, W.FP8, True, False), (257, W.FP8, False, False), (257, W.FP8, True, True),
     (257, W.BF16, True, False), (257, W.FP8_E8M0, True, False),
+    (257, W.FP8_E8M0_ROWS, True, False),
     (1500, W.FP8, True, False), (5000, W.FP8_E8M0, True, False)])
 def test_fused_decode_equals_three_calls(eg, B, dtype, with_history, in_place_history):
     """One new token a slot: the fused decode launch gives the streams and the

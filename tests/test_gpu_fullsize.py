@@ -64,7 +64,8 @@ def run_full(eg, cfg, device_inputs):
 def device_inputs(eg, cfg):
     import torch
     tabs, scales = W.tables_device(cfg, "cuda")
-    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16}[cfg.dtype]
+    dt = {W.FP8: eg.TABLE_FP8_E4M3FN, W.FP8_E8M0: eg.TABLE_FP8_E8M0, W.BF16: eg.TABLE_BF16,
+          W.FP8_E8M0_ROWS: eg.TABLE_FP8_E8M0_ROWS}[cfg.dtype]
     hist = W.history(cfg)
     pos, dead = W.packed_layout(cfg) if cfg.packed else (None, None)
     return dict(ids=torch.from_numpy(W.token_ids(cfg)).cuda(),
@@ -93,7 +94,8 @@ def check_streams(cfg, d, out, r_all, toks):
         t = d["tables"].tables[n].index_select(0, idx).cpu().numpy()
         tabs.append(t.view(np.uint16) if cfg.dtype == W.BF16 else t.view(np.uint8))
         scs.append(d["tables"].scales[n].index_select(0, idx).cpu().numpy()
-                   if cfg.dtype != W.BF16 else None)
+                   if cfg.dtype in (W.FP8, W.FP8_E8M0) else None)
+    tabs, scs = P.oracle_tables(cfg, tabs, scs)
     sel = torch.from_numpy(np.ascontiguousarray(toks)).cuda()
     x = d["streams"].view(T, 4, cfg.D)[sel].cpu().numpy().view(np.uint16)
     y_ref, f3 = oracle.lookup(remap, cfg.H, P.oracle_dtype(cfg), tabs, scs, x,
@@ -104,7 +106,8 @@ def check_streams(cfg, d, out, r_all, toks):
 
 
 @pytest.mark.parametrize("name", ["mid_prefill_fp8", "decode_fp8", "full_prefill_fp8", "bf16_tables",
-                                  "packed_mm_fp8", "full_prefill_fp8_e8m0", "release_layout_fp8"])
+                                  "packed_mm_fp8", "full_prefill_fp8_e8m0", "release_layout_fp8",
+                                  "release_layout_fp8_rows"])
 def test_full_size_sampled(eg, name):
     import torch
     cfg = W.by_name(name)

@@ -33,6 +33,12 @@ SMALL = {
                                       e8m0_lo=124, e8m0_hi=129),
     "e8m0_d96": C("full_prefill_fp8_e8m0").scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41)),
     "release_layout_d256": C("release_layout_fp8").scaled(B=2, S=333, rows=(32_000,) * 3, hash_vocab=1000),
+    "rows_layout_d256": C("release_layout_fp8_rows").scaled(B=2, S=333, rows=(32_000,) * 3,
+                                                             hash_vocab=1000),
+    "rows_e8m0_h8_d4096": C("full_prefill_fp8_e8m0").scaled(B=1, S=301, rows=(6007, 6011, 6029),
+                                                             dtype=W.FP8_E8M0_ROWS),
+    "rows_e8m0_d96": C("full_prefill_fp8_e8m0").scaled(B=1, S=50, H=3, D=96, rows=(31, 37, 41),
+                                                        dtype=W.FP8_E8M0_ROWS),
     "release_layout_d512_h4": C("release_layout_fp8").scaled(B=1, S=301, H=4, D=512, rows=(16_000,) * 3,
                                           hash_vocab=1000, e8m0_lo=124, e8m0_hi=129),
     "release_layout_bf16_d1024": C("release_layout_fp8").scaled(B=1, S=129, H=4, D=1024, rows=(16_000,) * 3,
@@ -106,3 +112,40 @@ def test_in_place_streams(eg, kernel, name):
     a = P.gpu_path(cfg, dev, aux=False)
     b = P.gpu_path(cfg, dev, aux=False, in_place=True)
     assert np.array_equal(a["streams"], b["streams"])
+
+
+@pytest.mark.parametrize("name", ["release_layout_d256", "e8m0_prefill_h8", "e8m0_d96",
+                                  "release_layout_d128_dead"])
+def test_rows_layout_equals_blocks_layout(eg, kernel, name):
+    """The same values with each row's exponents stored after its bytes
+    (TABLE_FP8_E8M0_ROWS) give the same bits as with the exponents apart, in
+    every lookup kernel; the packed tables come from engram_pack_e8m0_rows."""
+    import torch
+    cfg = SMALL[name]
+    dev = P.to_device(P.host_inputs(cfg))
+    a = P.gpu_path(cfg, dev, aux=True)
+    packed = [eg.engram_pack_e8m0_rows(t, s) for t, s in zip(dev["tables"].tables,
+                                                              dev["tables"].scales)]
+    dev["tables"] = eg.Tables(eg.TABLE_FP8_E8M0_ROWS, packed, None)
+    b = P.gpu_path(cfg, dev, aux=True)
+    assert a["flags"] == b["flags"] == 0
+    for key in ("rows", "streams", "gate", "mem"):
+        assert np.array_equal(a[key], b[key]), key
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("D,rows", [(256, 1001), (4096, 37), (32, 5), (96, 2)])
+def test_pack_e8m0_rows_layout(eg, D, rows):
+    """engram_pack_e8m0_rows writes each row's bytes, then its D/32 exponents,
+    then zeros up to a multiple of 16 bytes."""
+    import torch
+    g = np.random.default_rng(D + rows)
+    t = g.integers(0, 256, size=(rows, D), dtype=np.uint8)
+    e = g.integers(0, 256, size=(rows, D // 32), dtype=np.uint8)
+    out = torch.full((rows, eg.e8m0_row_bytes(D)), 0xAB, dtype=torch.uint8, device="cuda")
+    eg.engram_pack_e8m0_rows(torch.from_numpy(t).cuda(), torch.from_numpy(e).cuda(), packed=out)
+    got = out.cpu().numpy()
+    assert got.shape[1] % 16 == 0 and got.shape[1] >= D + D // 32
+    assert np.array_equal(got[:, :D], t)
+    assert np.array_equal(got[:, D:D + D // 32], e)
+    assert np.all(got[:, D + D // 32:] == 0)

@@ -100,3 +100,19 @@ def test_packed_layout():
     assert 0.15 < frac < 0.3, frac
     plain_pos, plain_dead = W.packed_layout(W.by_name("full_prefill_fp8").scaled(B=2, S=64))
     assert np.array_equal(plain_pos[1], np.arange(64)) and not plain_dead.any()
+
+
+def test_rows_layout_holds_the_blocks_layout_values():
+    """The rows-with-exponents workload draws the same bytes and exponents as the
+    blocks layout and stores each row, then its exponents, then zeros; its
+    algorithmic bytes per token are the same (the padding is not counted)."""
+    e8 = W.by_name("release_layout_fp8").scaled(rows=(500,) * 3, hash_vocab=10)
+    rw = W.by_name("release_layout_fp8_rows").scaled(rows=(500,) * 3, hash_vocab=10)
+    (t,), (e,) = [x[:1] for x in W.tables_host(e8)]
+    (p,), _ = [x[:1] for x in W.tables_host(rw)]
+    D = rw.D
+    assert rw.stored_row_bytes() == 272 and p.shape == (500, 272)
+    assert np.array_equal(p[:, :D], t) and np.array_equal(p[:, D:D + D // 32], e)
+    assert not p[:, D + D // 32:].any()
+    assert rw.algorithmic_bytes_per_token() == e8.algorithmic_bytes_per_token()
+    assert W.by_name("release_layout_fp8_rows").table_bytes() == 384_006_168 * 272

@@ -33,6 +33,9 @@ _K_IDS, _K_MAP, _K_TABLE, _K_SCALE, _K_STREAMS, _K_ALPHA, _K_HIST, _K_SPANS, _K_
 FP8 = "fp8_e4m3fn"
 BF16 = "bf16"
 FP8_E8M0 = "fp8_e4m3fn_e8m0_1x32"   # one e8m0 exponent per row per 32 columns
+# the same values, each row's exponents stored right after its bytes (rows padded
+# to a multiple of 16 bytes)
+FP8_E8M0_ROWS = "fp8_e4m3fn_e8m0_1x32_rows"
 E4M3_MAX = 448.0
 
 
@@ -99,17 +102,24 @@ class EngramConfig:
 
     def row_bytes(self) -> int:
         """Bytes of one table row with its scales: FP8 D + 4 (fp32 row scale),
-        FP8 with e8m0 blocks D + D/32, BF16 2D."""
+        FP8 with e8m0 blocks D + D/32 (apart or after the row), BF16 2D."""
         if self.dtype == FP8:
             return self.D + 4
-        if self.dtype == FP8_E8M0:
+        if self.dtype in (FP8_E8M0, FP8_E8M0_ROWS):
             return self.D + self.D // 32
         return 2 * self.D
 
+    def stored_row_bytes(self) -> int:
+        """Bytes a table row takes in memory (the rows-with-exponents layout pads
+        each row to a multiple of 16 bytes)."""
+        if self.dtype == FP8_E8M0_ROWS:
+            return (self.D + self.D // 32 + 15) // 16 * 16
+        return self.row_bytes()
+
     def table_bytes(self) -> int:
         if self.hash_vocab:
-            return self.rows[0] * self.row_bytes()
-        return sum(r * self.row_bytes() for r in self.rows)
+            return self.rows[0] * self.stored_row_bytes()
+        return sum(r * self.stored_row_bytes() for r in self.rows)
 
     def algorithmic_bytes_per_token(self) -> int:
         """Bytes the fused lookup must move per token, with no cache credit:
@@ -154,6 +164,11 @@ CONFIGS = [
     EngramConfig(name="release_layout_fp8", seed=7, B=8, S=8192, vocab=129_280, n_eids=100_000,
                  H=8, D=256, rows=(384_006_168,) * 3, dtype=FP8_E8M0, ids="zipf",
                  repeat_frac=0.05, hash_vocab=16_000_000),
+    # 7b: the released table layout with each row's exponents stored after its
+    #     bytes (272-byte rows, 104 GB): the same seed, so the same values as 7
+    EngramConfig(name="release_layout_fp8_rows", seed=7, B=8, S=8192, vocab=129_280,
+                 n_eids=100_000, H=8, D=256, rows=(384_006_168,) * 3, dtype=FP8_E8M0_ROWS,
+                 ids="zipf", repeat_frac=0.05, hash_vocab=16_000_000),
     # 8: the connection with a wkv projection on the released table layout: a
     #    token's 24 rows of 256 (K = 6144) projected to the 4096-wide streams;
     #    wkv_std 2 gives k about the streams' unit scale (rows ~ 0.0045 rms)
@@ -305,11 +320,20 @@ def tables_host(cfg: EngramConfig):
             tabs.append(_to_e4m3_bytes(x))
             gs = rng(cfg, _K_SCALE, n)
             scales.append(gs.uniform(cfg.scale_lo, cfg.scale_hi, size=cfg.rows[n]).astype(np.float32))
-        elif cfg.dtype == FP8_E8M0:
-            tabs.append(_to_e4m3_bytes(x))
+        elif cfg.dtype in (FP8_E8M0, FP8_E8M0_ROWS):
+            t = _to_e4m3_bytes(x)
             gs = rng(cfg, _K_SCALE, n)
-            scales.append(gs.integers(cfg.e8m0_lo, cfg.e8m0_hi + 1, size=(cfg.rows[n], cfg.D // 32),
-                                      dtype=np.int64).astype(np.uint8))
+            e = gs.integers(cfg.e8m0_lo, cfg.e8m0_hi + 1, size=(cfg.rows[n], cfg.D // 32),
+                            dtype=np.int64).astype(np.uint8)
+            if cfg.dtype == FP8_E8M0:
+                tabs.append(t)
+                scales.append(e)
+            else:   # each row, then its exponents, then zeros
+                packed = np.zeros((cfg.rows[n], cfg.stored_row_bytes()), np.uint8)
+                packed[:, :cfg.D] = t
+                packed[:, cfg.D:cfg.D + cfg.D // 32] = e
+                tabs.append(packed)
+                scales.append(None)
         else:
             tabs.append(_to_bf16_bits(x * np.float32(cfg.bf16_std)))
             scales.append(None)
@@ -337,8 +361,11 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
     for n in range(1 if cfg.hash_vocab else 3):
         rows = cfg.rows[n]
         g = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 7)
-        fp8 = cfg.dtype in (FP8, FP8_E8M0)
-        if fp8:
+        fp8 = cfg.dtype in (FP8, FP8_E8M0, FP8_E8M0_ROWS)
+        packed = cfg.dtype == FP8_E8M0_ROWS
+        if packed:   # rows with their exponents after them: [rows, stored_row_bytes]
+            t = torch.zeros((rows, cfg.stored_row_bytes()), dtype=torch.uint8, device=device)
+        elif fp8:
             t = torch.empty((rows, cfg.D), dtype=torch.uint8, device=device)
         else:
             t = torch.empty((rows, cfg.D), dtype=torch.int16, device=device)
@@ -346,7 +373,7 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
             r1 = min(rows, r0 + chunk_rows)
             x = torch.randn((r1 - r0, cfg.D), generator=g, device=device, dtype=torch.float32)
             if fp8:
-                t[r0:r1] = x.clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+                t[r0:r1, :cfg.D] = x.clamp_(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
             else:
                 t[r0:r1] = x.mul_(cfg.bf16_std).to(torch.bfloat16).view(torch.int16)
             del x
@@ -360,6 +387,15 @@ def tables_device(cfg: EngramConfig, device, chunk_rows: int = 1 << 18):
             scales.append(torch.randint(cfg.e8m0_lo, cfg.e8m0_hi + 1, (rows, cfg.D // 32),
                                         generator=gs, device=device, dtype=torch.int32)
                           .to(torch.uint8))
+        elif packed:   # the same draws as FP8_E8M0, written after each row, in chunks
+            gs = _dev_gen(device, cfg.seed * 1_000_003 + 101 * n + 11)
+            e = torch.randint(cfg.e8m0_lo, cfg.e8m0_hi + 1, (rows, cfg.D // 32),
+                              generator=gs, device=device, dtype=torch.int32)
+            for r0 in range(0, rows, 1 << 24):
+                r1 = min(rows, r0 + (1 << 24))
+                t[r0:r1, cfg.D:cfg.D + cfg.D // 32] = e[r0:r1].to(torch.uint8)
+            del e
+            scales.append(None)
         else:
             scales.append(None)
     if cfg.hash_vocab:   # one table, shared by the three orders
