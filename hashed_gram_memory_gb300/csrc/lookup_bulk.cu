@@ -280,15 +280,18 @@ size_t small_smem_bytes(int D, int dtype, int H, int tpb) {
 }
 
 // Tokens per block, a whole number of warps.  Measured on the released shape
-// (256-wide FP8 rows with e8m0 blocks, 24 rows a token, 65,536 tokens): blocks
-// of three warps, five to an SM, took 157 us; every other size tried, from one
-// to seven warps a block and from two to sixteen blocks an SM (20 to 32 tokens
-// resident), took 166-197 us, the three-warp size with only four blocks an SM
-// among the slowest.  So: three warps when five such blocks fit in an SM's
-// 228 KB of shared memory (1 KB of each block's is reserved); else the largest
-// block of up to 256 threads within 56 KB (four blocks an SM).
+// (256-wide FP8 rows with e8m0 blocks, 24 rows a token, 65,536 tokens): with the
+// exponents apart, blocks of three warps, five to an SM, took 157 us; every
+// other size tried, from one to seven warps a block and from two to sixteen
+// blocks an SM (20 to 32 tokens resident), took 166-197 us, the three-warp size
+// with only four blocks an SM among the slowest.  So: three warps when five
+// such blocks fit in an SM's 228 KB of shared memory (1 KB of each block's is
+// reserved); else the largest block of up to 256 threads within 56 KB (four
+// blocks an SM).  With the exponents after each row, one warp a block measured
+// best (131.9 us against 133.7 / 135.1 / 138.3 us for two, three and four warps).
 int small_tokens_per_block(int D, int dtype, int H) {
   const int tpt = D / 16, warp_tokens = 32 / tpt;
+  if (dtype == ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS) return warp_tokens;
   if (small_smem_bytes(D, dtype, H, 3 * warp_tokens) + 1024 <= 228 * 1024 / 5)
     return 3 * warp_tokens;
   int tpb = 256 / tpt;
