@@ -374,3 +374,29 @@ def test_plain_c_program_links_and_runs(eg, tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     assert "FAIL" not in r.stdout and r.stdout.count("ok") >= 9
 
+
+
+def test_rows_layout_and_packing_argument_errors(eg):
+    """Tables whose rows carry their e8m0 exponents, and engram_pack_e8m0_rows:
+    every argument error returns before a launch."""
+    L = eg.lib
+    INV = eg.ERR_INVALID_ARG
+    x, y, a, ids = C.c_void_p(0x100000000), C.c_void_p(0x200000000), C.c_void_p(0x3000), C.c_void_p(0x4000)
+    # D % 32 != 0 is refused; a rows-layout table needs no scales (an empty call is OK)
+    bad = _tables(dtype=eg.TABLE_FP8_E8M0_ROWS, D=48, scale=0)
+    assert L.engram_lookup_fused(ids, 8, 2, C.byref(bad), x, y, a, 1e-6, None, None, None, None) == INV
+    assert b"32" in L.engram_last_error()
+    ok = _tables(dtype=eg.TABLE_FP8_E8M0_ROWS, D=256, scale=0)
+    assert L.engram_lookup_fused(ids, 0, 2, C.byref(ok), None, None, a, 1e-6, None, None, None,
+                                 None) == eg.OK
+    # the rows-layout macro and the binding agree
+    assert [eg.e8m0_row_bytes(D) for D in (32, 256, 4096)] == [48, 272, 4224]
+    p, e, q = C.c_void_p(0x10000), C.c_void_p(0x80000), C.c_void_p(0x100000)
+    assert L.engram_pack_e8m0_rows(p, e, 10, 48, q, None) == INV          # D % 32
+    assert L.engram_pack_e8m0_rows(p, e, 10, 8192, q, None) == INV        # D > ENGRAM_MAX_D
+    assert L.engram_pack_e8m0_rows(p, e, -1, 256, q, None) == INV         # rows < 0
+    assert L.engram_pack_e8m0_rows(None, e, 10, 256, q, None) == INV      # NULL table
+    assert L.engram_pack_e8m0_rows(p, e, 10, 256, C.c_void_p(0x100008), None) == INV  # misaligned
+    assert L.engram_pack_e8m0_rows(p, e, 10, 256, C.c_void_p(0x10100), None) == INV   # overlaps table
+    assert b"overlaps" in L.engram_last_error()
+    assert L.engram_pack_e8m0_rows(None, None, 0, 256, None, None) == eg.OK  # nothing to do
