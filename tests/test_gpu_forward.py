@@ -177,3 +177,68 @@ def test_fused_decode_bad_token_leaves_its_slot_unwritten(eg):
                              history_out=torch.empty_like(hist))
     keep = [b for b in range(cfg.B) if b != 10]
     assert torch.equal(out[keep], good[keep])
+
+
+@pytest.mark.parametrize("mode", ["queued", "graph"])
+def test_back_to_back_decode_steps_equal_synchronised_steps(eg, mode):
+    """Sixteen decode steps chained through one history and one set of streams,
+    both updated in place, so that every step reads what the step before wrote.
+    The fused decode launch lets the next grid start while the previous one
+    finishes (programmatic dependent launch); launched back to back (queued
+    behind a sleeping kernel, or replayed from a CUDA graph) the steps must give
+    the bits of the same steps with a synchronize after each, and the history
+    the oracle's hash chain gives."""
+    import torch
+    import oracle
+    cfg = W.by_name("decode_fp8").scaled(B=77, rows=(7001, 7013, 7019))
+    inp = P.host_inputs(cfg)
+    dev = P.to_device(inp)
+    N = 16
+    ids_h = [W.token_ids(cfg, 100 + s) for s in range(N)]
+    ids = [torch.from_numpy(a).cuda() for a in ids_h]
+    ws = torch.empty(max(eg.engram_forward_workspace_bytes(cfg.B, 1, cfg.H), 16),
+                     dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = torch.empty_like(dev["streams"])
+    h = torch.empty_like(dev["history"])
+
+    def reset():
+        x.copy_(dev["streams"])
+        h.copy_(dev["history"])
+
+    def steps(sync):
+        for s in range(N):
+            eg.engram_forward(ids[s], dev["tid2eid"], cfg.n_eids, cfg.H, dev["tables"], x,
+                              dev["alpha"], cfg.eps, history=h, history_out=h, streams_out=x,
+                              workspace=ws, status=st)
+            if sync:
+                torch.cuda.synchronize()
+
+    reset()
+    torch.cuda.synchronize()
+    steps(sync=True)
+    x_ref, h_ref = x.clone(), h.clone()
+
+    reset()
+    if mode == "queued":
+        torch.cuda._sleep(20_000_000)  # every launch below is queued before the first runs
+        steps(sync=False)
+    else:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            steps(sync=False)
+        reset()
+        g.replay()
+    torch.cuda.synchronize()
+    assert eg.engram_read_status(st)[1] == 0
+    assert torch.equal(h, h_ref)
+    assert torch.equal(x, x_ref)
+
+    hist = inp.history
+    for a in ids_h:
+        e, f1 = oracle.compress(a, inp.tid2eid, cfg.n_eids)
+        _, hist, f2 = oracle.hash_ids(e, cfg.H, cfg.rows, history=hist, want_history=True)
+        assert f1 == f2 == 0
+    assert np.array_equal(h.cpu().numpy(), hist)
