@@ -64,13 +64,13 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Polls the phase with parity 0 of `bar` until it completes (true) or limit_ns
-// passes (false).
-__device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns) {
-  if (mbar_try_wait(bar, 0)) return true;
+// Polls the phase of `bar` with parity `parity` until it completes (true) or
+// limit_ns passes (false).
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, int64_t limit_ns, uint32_t parity = 0) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
-    if (mbar_try_wait(bar, 0)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((int64_t)(global_ns() - t0) > limit_ns) return false;
   }
 }

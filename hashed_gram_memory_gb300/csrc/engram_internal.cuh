@@ -77,7 +77,7 @@ struct LookupParams {
   int64_t T;
   int32_t H, D;
   int32_t tpt;  // gather kernel: threads per token (16 columns each)
-  int32_t tpb;  // gather kernel: tokens per block
+  int32_t tpb;  // tokens per block (gather, small-row and chained bulk kernels)
   int32_t withhold; // test hook: withhold one row copy per block (bulk kernels, decode step)
   int64_t wait_limit_ns;
   float eps, inv_R, inv_D, sqrt_D;

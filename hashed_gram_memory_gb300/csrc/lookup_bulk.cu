@@ -39,6 +39,74 @@ __global__ void __launch_bounds__(256, EARLY ? 2 : 4)
   bulk_token<DT, AUX, EARLY>(p, p.row_ids + t * 3 * p.H, t);
 }
 
+// Large tokens (two blocks per SM, streams loaded early): p.tpb consecutive
+// tokens a block, one after the other.  As soon as every thread has read a
+// token's rows from shared memory, warp 0 issues the next token's row copies,
+// which then fly under the current token's gate and stores; the next token's
+// scales are loaded after those stores, under its copies.  A block thus keeps
+// its rows in flight between tokens instead of ending and being replaced, and
+// a few tokens a block leave the hardware scheduler room to even out the SMs.
+// Each token's arithmetic is bulk_token's, so the results are the same bits.
+template <int DT, bool AUX>
+__global__ void __launch_bounds__(256, 2)
+    lookup_bulk_chain_kernel(const __grid_constant__ LookupParams p) {
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int R = 3 * p.H, tid = threadIdx.x;
+  const BulkSmem s = bulk_smem<DT>(sm, R, p.D);
+  if (tid == 0) {
+    mbar_init(s.bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const int64_t t0 = (int64_t)blockIdx.x * p.tpb;
+  const int64_t end = t0 + p.tpb < p.T ? t0 + p.tpb : p.T;
+  uint32_t phase = 0;  // parity of the barrier phase the current token's copies complete
+  int64_t t = t0;
+  int state = bulk_state(p, p.row_ids + t * R);  // its barrier publishes the mbarrier's set-up
+  if (state == kBulkLive) {
+    bulk_issue_rows<true>(p, p.row_ids + t * R, t, s);
+    bulk_load_scales<DT>(p, p.row_ids + t * R, s);
+  }
+  for (;;) {
+    const int64_t tn = t + 1;
+    const int32_t *ids_n = p.row_ids + tn * R;
+    int next = kBulkBad;  // no next token
+    if (state == kBulkLive) {
+      uint4 xs[4][2];
+      bulk_load_streams(p.x + t * 4 * p.D + tid * 16, p.D, xs);
+      const bool landed = wait_bounded(s.bar, p.wait_limit_ns, phase);
+      // Block-uniform outcome; the barrier also publishes the scales.
+      if (__syncthreads_or(!landed)) {
+        if (tid == 0) {
+          if (p.status) atomicOr(p.status, ENGRAM_FLAG_TIMEOUT);
+          wait_bounded(s.bar, p.wait_limit_ns, phase);  // let the issued copies land before exit
+        }
+        return;  // this token and the block's later ones stay unwritten
+      }
+      phase ^= 1;
+      float acc[16];
+      bulk_accumulate<DT>(p, s, tid * 16, acc);
+      if (tn < end) {
+        next = bulk_state(p, ids_n);  // its barrier: every thread is done with the rows
+        if (next == kBulkLive) bulk_issue_rows<true>(p, ids_n, tn, s);
+      }
+      bulk_gate_store<AUX, true>(p, t, s, xs, acc);
+      if (next == kBulkLive) bulk_load_scales<DT>(p, ids_n, s);
+    } else {
+      if (state == kBulkDead) bulk_pass_through<AUX>(p, t);
+      if (tn < end) {
+        next = bulk_state(p, ids_n);
+        if (next == kBulkLive) {
+          bulk_issue_rows<true>(p, ids_n, tn, s);
+          bulk_load_scales<DT>(p, ids_n, s);
+        }
+      }
+    }
+    if (tn >= end) return;
+    t = tn;
+    state = next;
+  }
+}
+
 // A row's e8m0 exponents, n = D/32 bytes with n in {1, 2, 4, 8} (the small-row
 // kernel's widths), as one naturally aligned load and store.
 __device__ __forceinline__ uint64_t load_exps(const uint8_t *e, uint32_t n) {
@@ -250,12 +318,38 @@ cudaError_t launch_bulk_t(const LookupParams &p, size_t smem, cudaStream_t strea
   return cudaGetLastError();
 }
 
+// Tokens a block of the chained kernel: 4, fewer when that would leave part of
+// the first wave of blocks empty.  Measured on the 8-head FP8 prefill (65,536
+// tokens): 1 (a token a block) 1.649 ms; 4 1.625; 8 1.626; 16 1.636; 32 1.658;
+// a single wave of blocks 1.649.  BF16 rows: 0.782 / 0.762 / 0.768 / 0.778 /
+// 0.825 ms; the packed batch: 1.581 / 1.488 / 1.474 / 1.489 / 1.530 ms.
+constexpr int kChainTokens = 4;
+
+template <int DT, bool AUX>
+cudaError_t launch_chain_t(const LookupParams &p_in, size_t smem, cudaStream_t stream) {
+  auto kern = lookup_bulk_chain_kernel<DT, AUX>;
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = raise_smem_ceiling(kern, configured);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, p_in.D / 16, smem);
+  if (e != cudaSuccess) return e;
+  LookupParams p = p_in;
+  const int64_t wave = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+  const int64_t fill = p.T / wave;  // tokens a block that still fill the first wave
+  p.tpb = (int)(fill < 1 ? 1 : fill < kChainTokens ? fill : kChainTokens);
+  const int64_t blocks = (p.T + p.tpb - 1) / p.tpb;
+  kern<<<(unsigned)blocks, p.D / 16, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int DT>
 cudaError_t launch_bulk_dt(const LookupParams &p, size_t smem, bool aux, bool early,
                            cudaStream_t stream) {
   if (early)
-    return aux ? launch_bulk_t<DT, true, true>(p, smem, stream)
-               : launch_bulk_t<DT, false, true>(p, smem, stream);
+    return aux ? launch_chain_t<DT, true>(p, smem, stream) : launch_chain_t<DT, false>(p, smem, stream);
   return aux ? launch_bulk_t<DT, true, false>(p, smem, stream)
              : launch_bulk_t<DT, false, false>(p, smem, stream);
 }
