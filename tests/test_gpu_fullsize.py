@@ -106,7 +106,8 @@ def check_streams(cfg, d, out, r_all, toks):
 
 
 @pytest.mark.parametrize("name", ["mid_prefill_fp8", "decode_fp8", "full_prefill_fp8", "bf16_tables",
-                                  "packed_mm_fp8", "full_prefill_fp8_e8m0", "release_layout_fp8",
+                                  "packed_mm_fp8", "full_prefill_fp8_e8m0",
+                                  "full_prefill_fp8_e8m0_rows", "release_layout_fp8",
                                   "release_layout_fp8_rows"])
 def test_full_size_sampled(eg, name):
     import torch

@@ -158,6 +158,11 @@ CONFIGS = [
     EngramConfig(name="full_prefill_fp8_e8m0", seed=6, B=8, S=8192, vocab=129_280,
                  n_eids=100_000, H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8_E8M0, ids="zipf",
                  repeat_frac=0.05),
+    # 6b: the same tables with each row's exponents stored after its bytes
+    #     (4224-byte rows): the same seed, so the same values as 6
+    EngramConfig(name="full_prefill_fp8_e8m0_rows", seed=6, B=8, S=8192, vocab=129_280,
+                 n_eids=100_000, H=8, D=4096, rows=(5_040_000,) * 3, dtype=FP8_E8M0_ROWS,
+                 ids="zipf", repeat_frac=0.05),
     # 7: the released table layout: one Engram layer's table of 384,006,168 rows
     #    of 256 FP8 values with (1, 32) e8m0 blocks (98 GB), cut into 24 prime
     #    buckets (orders 2..4 x 8 heads) drawn above a 16,000,000 hash vocabulary
