@@ -149,3 +149,43 @@ def test_pack_e8m0_rows_layout(eg, D, rows):
     assert np.array_equal(got[:, :D], t)
     assert np.array_equal(got[:, D:D + D // 32], e)
     assert np.all(got[:, D + D // 32:] == 0)
+
+
+@pytest.mark.parametrize("D,H", [(256, 1), (4096, 5)])
+@pytest.mark.parametrize("layout", ["apart", "rows"])
+def test_every_e8m0_exponent_value(eg, kernel, D, H, layout):
+    """Every e8m0 exponent byte 0..255 through the lookup: token t reads row t in
+    every head of the three tables, whose FP8 values are all 2^-5 (0x10) and
+    whose (1, 32) blocks carry the exponents 0..255 in turn.  The memory m of
+    each block is then exactly (3H * 2^-5 * 2^(e-127)) * fl32(1/3H), which
+    numpy's fp32 product gives; e = 0 is the subnormal 2^-127, e = 255 NaN (OCP
+    MX E8M0, the release's (1, 32) blocks: VeOmni PR page, commit "Two things
+    stopped the real conversion").  For the small-row, one-token-a-block or
+    chained and register-gather kernels, exponents apart or after each row."""
+    import torch
+    nb = D // 32                     # blocks (exponents) a row
+    T = 256 // nb                    # rows = tokens, all 256 values once
+    R = 3 * H
+    tab = torch.full((T, D), 0x10, dtype=torch.uint8, device="cuda")
+    e = np.arange(256, dtype=np.uint8).reshape(T, nb)
+    exps = torch.from_numpy(e).cuda()
+    if layout == "rows":
+        packed = eg.engram_pack_e8m0_rows(tab, exps)
+        tables = eg.Tables(eg.TABLE_FP8_E8M0_ROWS, [packed] * 3, None)
+    else:
+        tables = eg.Tables(eg.TABLE_FP8_E8M0, [tab] * 3, [exps] * 3)
+    ids = torch.arange(T, dtype=torch.int32, device="cuda").view(T, 1).expand(T, R).contiguous()
+    x = torch.zeros((T, 4, D), dtype=torch.int16, device="cuda")
+    alpha = torch.zeros(4, dtype=torch.float32, device="cuda")
+    mem = torch.empty((T, D), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    eg.engram_lookup_fused(ids, H, tables, x, alpha, 1e-6, mem_out=mem, status=st)
+    torch.cuda.synchronize()
+    assert eg.engram_read_status(st)[1] == 0
+    got = mem.cpu().numpy().reshape(256, 32)          # a block's 32 columns, one block per exponent
+    ev = np.arange(255)
+    acc = np.float32(R * 2.0 ** -5) * np.ldexp(np.float32(1.0), ev - 127).astype(np.float32)
+    want = (acc * (np.float32(1.0) / np.float32(R))).astype(np.float32)
+    bad = np.nonzero((got[:255].view(np.uint32) != want[:, None].view(np.uint32)).any(axis=1))[0]
+    assert bad.size == 0, f"exponents {bad[:8]}: {got[bad[:8], 0]} against {want[bad[:8]]}"
+    assert np.isnan(got[255]).all()
