@@ -1,7 +1,7 @@
 // lookup_bulk.cu -- the fused Engram lookup with the table rows staged in shared
 // memory by 1-D bulk copies (TMA), for sm_103a.
 //
-// One token per CTA of D/16 threads (16 columns each).  Warp 0 issues all 3H
+// A token is handled by a CTA of D/16 threads (16 columns each).  Warp 0 issues all 3H
 // row copies of the token at once, lane r the copy of row r (one contiguous
 // D*elt-byte run per row, one cp.async.bulk each, from an id the lane holds in a
 // register), completing on a single mbarrier that expects their total byte
@@ -13,13 +13,17 @@
 // are reduced across warps, and the four streams are written back with
 // evict-first stores.  A whole token is in flight from one warp's issue and the
 // rows cost no registers.  Two variants, chosen by the size of a token's
-// rows: two blocks per SM with the streams loaded early (8 heads of FP8 at
-// D = 4096: 96 KB of rows), or four blocks per SM within 64 registers with the
-// streams loaded after the rows (rows within 56 KB).
+// rows: for large tokens (8 heads of FP8 at D = 4096: 96 KB of rows) two blocks
+// per SM with the streams loaded early, each block running a few tokens in
+// turn with the next token's copies issued under the current token's gate and
+// stores (lookup_bulk_chain_kernel); for rows within 56 KB, one token a block,
+// four blocks per SM within 64 registers with the streams loaded after the
+// rows (lookup_bulk_kernel).
 //
 // The wait is bounded by the global timer: a copy that never lands makes the
-// block set ENGRAM_FLAG_TIMEOUT, skip the token, and exit only after thread 0
-// has waited (again bounded) for the copies warp 0 issued.  An id outside its table
+// block set ENGRAM_FLAG_TIMEOUT, skip the token (and a chained block its later
+// tokens), and exit only after thread 0 has waited (again bounded) for the
+// copies warp 0 issued.  An id outside its table
 // makes the block set ENGRAM_FLAG_BAD_ROW and skip the token before anything
 // is copied; a dead token (all ids ENGRAM_ROW_DEAD) copies its streams through.
 #include <atomic>
