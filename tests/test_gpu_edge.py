@@ -99,6 +99,48 @@ def test_lookup_flags_bad_rows_and_leaves_token_unwritten(eg):
     P.compare_streams(got[keep], ref[keep], inp.streams.reshape(cfg.T, 4, cfg.D)[keep])
 
 
+@pytest.mark.parametrize("H", [4, 8])
+def test_bad_rows_in_large_tokens_leave_exactly_those_tokens_unwritten(eg, H):
+    """4096-wide rows: one token a block (4 heads) and four tokens chained in a
+    block (8 heads, 1300 tokens).  Tokens with an id past its table, a negative
+    id, or dead ids mixed with live ones -- first, second, third and last in a
+    chained block, and the sequence's last token -- flag ENGRAM_FLAG_BAD_ROW and
+    stay unwritten; a fully dead token in a chain copies its streams through;
+    every other token equals the oracle."""
+    import torch
+    cfg = W.by_name("full_prefill_fp8").scaled(B=1, S=1300, H=H, rows=(1009, 1013, 1019))
+    inp = P.host_inputs(cfg)
+    eids, _ = oracle.compress(inp.ids, inp.tid2eid, cfg.n_eids)
+    rows, _ = oracle.hash_ids(eids, cfg.H, cfg.rows)
+    rows = rows.reshape(cfg.T, -1).copy()
+    bad = {4: ("past", 0), 9: ("neg", 7), 14: ("mix", 3), 7: ("past", 3 * H - 1),
+           cfg.T - 1: ("neg", 2)}
+    for t, (kind, r) in bad.items():
+        if kind == "past":
+            rows[t, r] = cfg.rows[r // H]
+        elif kind == "neg":
+            rows[t, r] = -2
+        else:
+            rows[t, :r] = oracle.DEAD
+    rows[21, :] = oracle.DEAD          # a dead token: streams copied through
+    ref, _, _, rflags = oracle.lookup(rows, cfg.H, oracle.FP8, inp.tables, inp.scales,
+                                      inp.streams.reshape(cfg.T, 4, cfg.D), inp.alpha, cfg.eps,
+                                      aux=True, fill=0x1234)
+    dev = P.to_device(inp)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((cfg.T, 4, cfg.D), 0x1234, dtype=torch.int16, device="cuda")
+    eg.engram_lookup_fused(_t(rows), cfg.H, dev["tables"], dev["streams"].view(cfg.T, 4, cfg.D),
+                           dev["alpha"], cfg.eps, streams_out=out, status=st)
+    code, flags = eg.engram_read_status(st)
+    assert code == eg.ERR_OUT_OF_RANGE and flags == rflags == eg.FLAG_BAD_ROW
+    got = out.cpu().numpy().view(np.uint16)
+    for t in bad:
+        assert (got[t] == 0x1234).all(), f"bad token {t} was written"
+    assert np.array_equal(got[21], inp.streams.reshape(cfg.T, 4, cfg.D)[21])
+    keep = [t for t in range(cfg.T) if t not in bad]
+    P.compare_streams(got[keep], ref[keep], inp.streams.reshape(cfg.T, 4, cfg.D)[keep])
+
+
 @pytest.mark.parametrize("split", [0, 1, 2, 3, 9])
 def test_decode_steps_in_place_history_equal_prefill(eg, split):
     import torch
