@@ -532,11 +532,14 @@ ENGRAM_API engram_status engram_read_status(const int32_t *status, int32_t *flag
  *   ENGRAM_LOOKUP_AUTO    the library picks (default: BULK where it applies);
  *   ENGRAM_LOOKUP_GATHER  register-direct gathers, one token per thread group,
  *                         rows loaded in batches of 8 (any D);
- *   ENGRAM_LOOKUP_BULK    one token per block: one thread stages all 3H rows in
- *                         shared memory with 1-D bulk copies (TMA) on a single
- *                         mbarrier while the others load the streams; needs
- *                         D % 512 == 0 and 3H*D*elt <= ~227 KB, otherwise the
- *                         call falls back to GATHER.
+ *   ENGRAM_LOOKUP_BULK    a token's 3H rows staged in shared memory by 1-D bulk
+ *                         copies (TMA) on an mbarrier while the threads load
+ *                         the scales and streams: for D % 512 == 0 a token a
+ *                         block of D/16 threads (a few tokens in turn a block
+ *                         when a token's rows exceed 56 KB), for D < 512 with
+ *                         D/16 a power of two several tokens a block; the
+ *                         token's rows must fit ~227 KB of shared memory,
+ *                         otherwise the call falls back to GATHER.
  * Both give identical results.  Returns the previous setting, or -1 for an
  * unknown value (nothing changed).  Not synchronised with calls in flight on
  * other host threads.
