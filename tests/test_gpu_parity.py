@@ -151,7 +151,7 @@ def test_pack_e8m0_rows_layout(eg, D, rows):
     assert np.all(got[:, D + D // 32:] == 0)
 
 
-@pytest.mark.parametrize("D,H", [(256, 1), (4096, 5)])
+@pytest.mark.parametrize("D,H", [(256, 1), (4096, 3), (4096, 5)])
 @pytest.mark.parametrize("layout", ["apart", "rows"])
 def test_every_e8m0_exponent_value(eg, kernel, D, H, layout):
     """Every e8m0 exponent byte 0..255 through the lookup: token t reads row t in
@@ -160,8 +160,9 @@ def test_every_e8m0_exponent_value(eg, kernel, D, H, layout):
     each block is then exactly (3H * 2^-5 * 2^(e-127)) * fl32(1/3H), which
     numpy's fp32 product gives; e = 0 is the subnormal 2^-127, e = 255 NaN (OCP
     MX E8M0, the release's (1, 32) blocks: VeOmni PR page, commit "Two things
-    stopped the real conversion").  For the small-row, one-token-a-block or
-    chained and register-gather kernels, exponents apart or after each row."""
+    stopped the real conversion").  Through the small-row (D 256), one-token-a-
+    block (3 heads at D 4096), chained (5 heads) and register-gather kernels,
+    with the exponents apart or after each row."""
     import torch
     nb = D // 32                     # blocks (exponents) a row
     T = 256 // nb                    # rows = tokens, all 256 values once
