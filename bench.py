@@ -53,17 +53,23 @@ REPLAYS_PER_ROUND = 8
 
 
 def parse():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap = argparse.ArgumentParser(description="One JSON line: the Engram step's tokens/s, the "
+                                 "dominant kernel against its roofline, end to end through "
+                                 "host buffers, and the CPU oracle's throughput.")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="ranks (one GPU each, launched by torchrun; replicas, weak scaling)")
+    ap.add_argument("--steps", type=int, default=1000, help="K: steps in each timed replay")
+    ap.add_argument("--warmup", type=int, default=20, help="untimed steps first (at least 3)")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"],
+                    help="reference: the CPU oracle alone, on the host cores")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=[c.name for c in W.CONFIGS])
-    ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-sample-tokens", type=int, default=32768)
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10,
+                    help="steps of each end-to-end round through host buffers")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32768,
+                    help="tokens (whole sequences) the oracle is timed on")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle's timing")
     ap.add_argument("--eager", action="store_true",
                     help="launch every timed step from Python instead of replaying the K steps "
                          "captured in one CUDA graph")
@@ -74,7 +80,8 @@ def parse():
     ap.add_argument("--hash-vocab", type=int, default=0,
                     help="override the bucketed layout's hash vocabulary (the table shrinks to "
                          "the sum of its buckets; small cases for ncu captures)")
-    ap.add_argument("--lookup-kernel", default="auto", choices=["auto", "gather", "bulk"])
+    ap.add_argument("--lookup-kernel", default="auto", choices=["auto", "gather", "bulk"],
+                    help="engram_set_lookup_kernel's choice for the lookup")
     ap.add_argument("--min-timed-s", type=float, default=MIN_TIMED_S,
                     help="replay the K timed steps until the timed region lasts this long")
     return ap.parse_args()
