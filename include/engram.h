@@ -293,7 +293,7 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
  * no formula; this library reads it as, per token with K = 3*n_heads*d:
  *   e     = the 3*n_heads dequantised rows concatenated in (order, head) order,
  *           K values, each exact in bf16 (BF16 tables, or FP8 e4m3fn with
- *           (1, 32) e8m0 block exponents)
+ *           (1, 32) e8m0 block exponents, apart or after each row)
  *   k     = wkv e, fp32 accumulation on the tensor cores (wkv bf16 [D, K],
  *           row j = output j's weights)
  *   g     = sigmoid(<rmsnorm(stream0), rmsnorm(k)> / sqrt(D)), as above with k
@@ -303,8 +303,9 @@ ENGRAM_API engram_status engram_lookup_fused(const int32_t *row_ids, int64_t n_t
  * k = E wkv^T (tcgen05 tensor cores, TMA, fp32 in tensor memory), then the gate
  * and the add.
  *   row_ids      int32 [n_tokens, 3*n_heads], as for engram_lookup_fused
- *   tables_host  dtype ENGRAM_TABLE_BF16 or ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32;
- *                D (the row width d) a multiple of 32
+ *   tables_host  dtype ENGRAM_TABLE_BF16, ENGRAM_TABLE_FP8_E4M3FN_E8M0_B32 or
+ *                ENGRAM_TABLE_FP8_E4M3FN_E8M0_ROWS; D (the row width d) a
+ *                multiple of 32
  *   wkv          bf16 bits [D, K], 16-byte aligned; D a multiple of 256 in
  *                [256, 8192] and K a multiple of 64
  *   streams_in / streams_out / alpha / eps / gate_out as engram_lookup_fused
