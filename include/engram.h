@@ -390,11 +390,14 @@ typedef struct engram_layout {
  * engram_forward_workspace_bytes(batch, seq, n_heads) bytes, 16-byte aligned,
  * owned by the caller, not read after the call's kernels end).
  * A decode step (seq == 1) whose rows the bulk lookup takes (D a multiple of
- * 512) runs as one fused launch instead: each slot's block compresses its
- * token, hashes its window into row ids kept on chip, and looks them up, with
- * results identical to the three calls; a bad token id, map value or history
- * id then flags the status word and leaves all of that slot's outputs
- * (streams, history_out) unwritten.
+ * 512, a token's rows within shared memory) runs as one fused launch instead:
+ * each slot's block compresses its token, hashes its window into row ids kept
+ * on chip, and looks them up, with results identical to the three calls; a bad
+ * token id, map value or history id then flags the status word and leaves all
+ * of that slot's outputs (streams, history_out) unwritten.  That launch allows
+ * programmatic dependent launch: its blocks may be scheduled while the kernel
+ * before it on `stream` finishes, and wait for that kernel to complete before
+ * touching memory, so the ordering on `stream` is as for any launch.
  *   token_ids int32 [batch, seq] (device); history / history_out as in
  *   engram_hash; layout_host as above (may be NULL); streams as in
  *   engram_lookup_fused ([batch*seq, 4, D]).
