@@ -622,14 +622,15 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-E2E_ROUNDS = 5
+E2E_ROUNDS = 9
 
 
 def timed_rounds(one, stream, steps, device):
     """Times E2E_ROUNDS rounds of `steps` calls of one() (host timer, a stream
     sync at the end of each round, max over ranks) and returns the median round
-    and all rounds: up to two rounds caught by a transient on the host (other
-    jobs share the machine's host memory) do not decide the figure."""
+    and all rounds: up to four rounds caught by a transient on the host (other
+    jobs share the machine's host memory and link; such rounds run at about half
+    the speed) do not decide the figure."""
     from hashed_gram_memory_gb300.replicas import max_over_ranks
     rounds = []
     for _ in range(E2E_ROUNDS):
@@ -695,7 +696,7 @@ def run_e2e(eg, cfg, step, stream, steps, world, device):
             "how": "engram_forward_host: pinned host ids (+ positions, dead mask) + streams in, "
                    "compress/hash/lookup, streams out; 2048-token chunks, copies overlapped with "
                    "the lookup on two copy streams; host timer around the steps + a final stream "
-                   "sync; the median of five rounds"}
+                   "sync; the median of nine rounds"}
 
 
 def run_e2e_connection(eg, cfg, step, stream, steps, world, device):
@@ -734,7 +735,7 @@ def run_e2e_connection(eg, cfg, step, stream, steps, world, device):
             "how": "engram_connection_host: pinned host ids + streams in, compress / hash, then "
                    "concat / projection / gate + add in 8192-token chunks between the copies of "
                    "their streams in and out (two copy streams, overlapped); host timer around "
-                   "the steps + a final stream sync; the median of five rounds"}
+                   "the steps + a final stream sync; the median of nine rounds"}
 
 
 # ----------------------------------------------------------------- CPU oracle
